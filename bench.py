@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the DFlash 2 draft tail on one GB300 (one rank per GPU).
+
+A step is one pass of the whole hot path over one draft block: the fused tail
+(top-16 -> pair scores -> walk) plus the 20 two-tap conv calls of the drafter
+(5 layers x 4 insertion points).  The headline workload is the 4B-drafter
+block at batch 1 (B=1, L=16, V=151,936, d=2560): value = microseconds per draft
+block.  The batched serving block (B=64) is measured in the same run and
+reported as blocks/s and HBM GB/s against the roofline.
+
+Timing: CUDA events on the launching stream around each step (a CUDA graph
+replay of the step), L2 flushed by a 256 MB write between steps, the GPU kept
+busy with a sleep kernel while the host enqueues so no host latency is timed.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from draft_selection_gb300 import workloads as wl  # noqa: E402
+
+HEADLINE = "drafter4b_l16"
+BATCHED = "serving_b64"
+METRIC = "µs per draft block at B=1; blocks/s and HBM GB/s vs roofline at B=64"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# --------------------------------------------------------------------------- bytes
+
+
+def tail_bytes(w: wl.Workload, es: int) -> dict:
+    """Algorithmic HBM bytes of one tail call, by kernel (each needed byte once)."""
+    R = w.rows
+    d = w.d
+    cand_rows = w.B * (16 * w.L + 1)
+    topk = R * w.V * es + R * 16 * 8
+    select = cand_rows * d * 2 + 3 * 256 * d * 2 + R * d * 2 + w.B * 4 + R * 16 * 8 + R * 256 * 4
+    walk = R * 16 * 4 + R * 16 * 4 + R * 4 + R * 16 * 4
+    return {"topk": topk, "select": select, "walk": walk, "total": topk + select + walk}
+
+
+def conv_bytes(w: wl.Workload) -> int:
+    d = w.d
+    return (2 * w.B * w.L * d * 2 + w.B * d * 2 + 2 * d * 4 + (2 * d // 16) * d * 2)
+
+
+def select_flops(w: wl.Workload) -> float:
+    return 2.0 * w.B * (16 * w.L + 1) * w.d * 512 + 2.0 * w.rows * w.d * 256
+
+
+def conv_flops(w: wl.Workload) -> float:
+    return 2.0 * w.B * w.L * w.d * (2 * w.d // 16)
+
+
+# --------------------------------------------------------------------------- setup
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join("/tmp", f"dfl2_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = float(parts[2])
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+class Case:
+    """One workload resident on the device, with its step as callables."""
+
+    def __init__(self, w: wl.Workload, T: float, device):
+        import draft_selection_gb300 as dfl2
+        self.dfl2 = dfl2
+        self.w, self.T = w, T
+        gen_dev = "cpu" if w.B == 1 else device
+        self.logits = wl.make_logits(w, gen_dev).to(device)
+        inp = wl.make_tail_inputs(w, gen_dev)
+        self.inp = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        self.seeds = torch.from_numpy(inp["seeds"].view(np.int64)).to(device)
+        self.convs = []
+        for k in range(w.conv_calls):
+            c = wl.make_conv_inputs(w, k, gen_dev)
+            c = {n: t.to(device) for n, t in c.items()}
+            c["y"] = torch.empty_like(c["x"])
+            self.convs.append(c)
+        B, L = w.B, w.L
+        self.tokens = torch.empty(B, L, dtype=torch.int32, device=device)
+        self.q = torch.empty(B, L, 16, dtype=torch.float32, device=device) if T > 0 else None
+        self.ws = dfl2.workspace(dfl2.dfl2_tail_workspace_size(B, L, w.V, w.d), device)
+        self.idx = torch.empty(B, L, 16, dtype=torch.int32, device=device)
+        self.val = torch.empty(B, L, 16, dtype=torch.float32, device=device)
+        self.scores = torch.empty(B, L, 16, 16, dtype=torch.float32, device=device)
+        self.ws_topk = dfl2.workspace(dfl2.dfl2_topk_workspace_size(B, L, w.V), device)
+        self.ws_sel = dfl2.workspace(dfl2.dfl2_select_workspace_size(B, L, w.d), device)
+        self.es = self.logits.element_size()
+
+    def tail(self):
+        i = self.inp
+        self.dfl2.dfl2_tail(self.logits, i["verified"], i["hidden"], i["E"], i["W_A"], i["W_B"],
+                            i["W_H"], self.T, self.seeds, 0, self.tokens, self.ws, q=self.q)
+
+    def conv(self, k=0):
+        c = self.convs[k]
+        self.dfl2.dfl2_conv2(c["x"], c["x_prev"], c["base"], c["W_c"], c["y"])
+
+    def convs20(self):
+        for k in range(len(self.convs)):
+            self.conv(k)
+
+    def step(self):
+        self.tail()
+        self.convs20()
+
+    def topk(self):
+        self.dfl2.dfl2_topk(self.logits, self.idx, self.val, self.ws_topk)
+
+    def select(self):
+        i = self.inp
+        self.dfl2.dfl2_select(self.idx, self.val, i["verified"], i["hidden"], i["E"], i["W_A"],
+                              i["W_B"], i["W_H"], self.scores, self.ws_sel)
+
+    def walk(self):
+        self.dfl2.dfl2_walk(self.scores, self.idx, self.T, self.seeds, 0, self.tokens, q=self.q)
+
+
+def capture(fn):
+    """CUDA graph of fn (warmed up twice first); returns (graph, kernels per replay)."""
+    import draft_selection_gb300 as dfl2
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = dfl2.dfl2_launch_count()
+    with torch.cuda.graph(g, stream=s, capture_error_mode="relaxed"):
+        fn()
+    torch.cuda.synchronize()
+    return g, dfl2.dfl2_launch_count() - n0
+
+
+def time_graph(g, steps, warmup, flush):
+    """Per-replay device time (ms) with L2 flushed before every replay."""
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for i in range(warmup + steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda._sleep(20000)  # keeps the GPU busy while the host enqueues the replay
+        if i >= warmup:
+            ev[i - warmup][0].record(stream)
+        g.replay()
+        if i >= warmup:
+            ev[i - warmup][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def summarize(ts):
+    return {"mean_ms": float(np.mean(ts)), "median_ms": float(np.median(ts)),
+            "min_ms": float(np.min(ts))}
+
+
+def roofline_obj(bytes_per_launch, ms, peak_gbs, which, traffic=None):
+    gbs = bytes_per_launch / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(gbs / peak_gbs, 4), "traffic": traffic, "peak_kind": which}
+
+
+# --------------------------------------------------------------------------- runs
+
+
+def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
+    w = case.w
+    tb = tail_bytes(w, case.es)
+    cb = conv_bytes(w)
+    g_step, k_step = capture(case.step)
+    g_tail, _ = capture(case.tail)
+    g_topk, _ = capture(case.topk)
+    case.topk()
+    g_sel, _ = capture(case.select)
+    case.select()
+    g_walk, _ = capture(case.walk)
+    g_conv, _ = capture(lambda: case.conv(0))
+    sub = max(3, min(steps, 400))
+    res = {"step": summarize(time_graph(g_step, steps, warmup, flush)),
+           "tail": summarize(time_graph(g_tail, sub, warmup, flush)),
+           "topk": summarize(time_graph(g_topk, sub, warmup, flush)),
+           "select": summarize(time_graph(g_sel, sub, warmup, flush)),
+           "walk": summarize(time_graph(g_walk, sub, warmup, flush)),
+           "conv": summarize(time_graph(g_conv, sub, warmup, flush))}
+    res["kernels_per_step"] = k_step
+    peak = pk["hbm_gbs"]
+    shares = {"topk": res["topk"]["mean_ms"], "select": res["select"]["mean_ms"],
+              "walk": res["walk"]["mean_ms"], "conv": res["conv"]["mean_ms"] * w.conv_calls}
+    dominant = max(shares, key=shares.get)
+    per_kernel = {
+        "topk": roofline_obj(tb["topk"], res["topk"]["mean_ms"], peak, which),
+        "select": roofline_obj(tb["select"], res["select"]["mean_ms"], peak, which),
+        "walk": roofline_obj(tb["walk"], res["walk"]["mean_ms"], peak, which),
+        "conv": roofline_obj(cb, res["conv"]["mean_ms"], peak, which),
+    }
+    per_kernel["select"]["tflops"] = round(select_flops(w) / (res["select"]["mean_ms"] * 1e-3)
+                                           / 1e12, 2)
+    per_kernel["conv"]["tflops"] = round(conv_flops(w) / (res["conv"]["mean_ms"] * 1e-3) / 1e12, 2)
+    res["shares_ms"] = shares
+    res["dominant"] = dominant
+    res["per_kernel"] = per_kernel
+    res["tail_bytes"] = tb["total"]
+    res["conv_bytes_per_call"] = cb
+    return res, g_step
+
+
+def measure_e2e(case: Case, g_step, steps, warmup, flush):
+    """The same step with the inputs copied from pinned host memory and the
+    result read back inside the timed region."""
+    host_in = [case.logits, case.inp["hidden"], case.inp["verified"], case.seeds]
+    for c in case.convs:
+        host_in += [c["x"], c["x_prev"]]
+    pinned = [t.detach().cpu().pin_memory() for t in host_in]
+    out_dev = [case.tokens] + ([case.q] if case.q is not None else [])
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out_dev]
+    h2d = sum(t.numel() * t.element_size() for t in pinned)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    stream = torch.cuda.current_stream()
+    ts = []
+    for i in range(warmup + steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda._sleep(20000)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for dst, src in zip(host_in, pinned):
+            dst.copy_(src, non_blocking=True)
+        g_step.replay()
+        for dst, src in zip(out_host, out_dev):
+            dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= warmup:
+            ts.append(a.elapsed_time(b))
+    return float(np.mean(ts)), h2d, d2h
+
+
+def cpu_baseline(case: Case, budget_s: float = 12.0):
+    """The oracle, as it stands, on this host's cores: whole draft blocks of the
+    same workload (tail + 20 conv calls) until the time budget is spent."""
+    import oracle
+    w = case.w
+    lg = wl.host(case.logits)
+    i = {k: (wl.host(v) if isinstance(v, torch.Tensor) else v) for k, v in case.inp.items()}
+    convs = [{k: wl.host(v) for k, v in c.items() if k != "y"} for c in case.convs]
+    n, t0 = 0, time.perf_counter()
+    while True:
+        idx, val = oracle.topk(lg, 16)
+        S = oracle.select(idx, val, i["verified"], i["hidden"], i["E"], i["W_A"], i["W_B"],
+                          i["W_H"])
+        oracle.walk(S, idx, case.T, i["seeds"], 0)
+        for c in convs:
+            oracle.conv2(c["x"], c["x_prev"], c["base"], c["W_c"])
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(dt / n * 1e6, 1), "unit": "µs per draft block",
+            "cores": oracle.get_threads(), "kind": "oracle",
+            "sample": f"{n} whole {w.name} blocks (tail + {w.conv_calls} conv calls), "
+                      f"{dt:.1f} s of host time"}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    w = wl.WORKLOADS[args.workload]
+    T = 1.0
+    lg = wl.host(wl.make_logits(w, "cpu"))
+    i = {k: (wl.host(v) if isinstance(v, torch.Tensor) else v)
+         for k, v in wl.make_tail_inputs(w, "cpu").items()}
+    convs = [{k: wl.host(v) for k, v in wl.make_conv_inputs(w, c, "cpu").items()}
+             for c in range(w.conv_calls)]
+
+    def block():
+        idx, val = oracle.topk(lg, 16)
+        S = oracle.select(idx, val, i["verified"], i["hidden"], i["E"], i["W_A"], i["W_B"],
+                          i["W_H"])
+        oracle.walk(S, idx, T, i["seeds"], 0)
+        for c in convs:
+            oracle.conv2(c["x"], c["x_prev"], c["base"], c["W_c"])
+
+    for _ in range(args.warmup):
+        block()
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        block()
+        ts.append(time.perf_counter() - t0)
+    us = float(np.mean(ts)) * 1e6
+    line = {"impl": "reference", "metric": METRIC, "value": round(us, 1),
+            "unit": "µs per draft block", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us / 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "d": w.d, "T": T,
+                       "conv_calls": w.conv_calls},
+            "cpu_baseline": {"value": round(us, 1), "unit": "µs per draft block",
+                             "cores": oracle.get_threads(), "kind": "oracle",
+                             "sample": f"{args.steps} whole {w.name} blocks per the step count"},
+            "e2e": {"value": round(us, 1), "unit": "µs per draft block",
+                    "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--batched", default=BATCHED, help="second workload ('' to skip)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    from draft_selection_gb300 import build
+    build.build()
+    import draft_selection_gb300 as dfl2
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pk, which = peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    w = wl.WORKLOADS[args.workload]
+    T = 1.0
+    case = Case(w, T, device)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    res, g_step = measure_native(case, args.steps, args.warmup, flush, pk, which)
+    step_ms = max_over_ranks(res["step"]["mean_ms"], world)
+    barrier(world)
+    e2e_ms, h2d, d2h = measure_e2e(case, g_step, max(3, min(args.steps, 200)), args.warmup, flush)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+
+    batched = None
+    if args.batched:
+        wb = wl.WORKLOADS[args.batched]
+        cb = Case(wb, 1.0, device)
+        rb, _ = measure_native(cb, max(3, min(args.steps, 200)), args.warmup, flush, pk, which)
+        tail_ms = max_over_ranks(rb["tail"]["mean_ms"], world)
+        step_b = max_over_ranks(rb["step"]["mean_ms"], world)
+        tb = tail_bytes(wb, cb.es)["total"]
+        batched = {
+            "workload": wb.name, "B": wb.B,
+            "blocks_per_s": round(world * wb.B / (step_b * 1e-3), 1),
+            "tail_blocks_per_s": round(world * wb.B / (tail_ms * 1e-3), 1),
+            "step_us": round(step_b * 1e3, 2), "tail_us": round(tail_ms * 1e3, 2),
+            "conv_us_per_call": round(rb["conv"]["mean_ms"] * 1e3, 2),
+            "tail_hbm_gbs": round(tb / (tail_ms * 1e-3) / 1e9, 1),
+            "tail_frac_of_hbm": round(tb / (tail_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+            "tail_bytes": tb,
+            "roofline": rb["per_kernel"][rb["dominant"]] | {"kernel": rb["dominant"]},
+            "per_kernel": rb["per_kernel"],
+            "kernel_ms": {k: round(rb[k]["mean_ms"], 5) for k in
+                          ("topk", "select", "walk", "conv")},
+        }
+        del cb
+    clk = clocks.stop()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case, args.cpu_budget)
+
+    if rank == 0:
+        us_block = step_ms * 1e3 / world
+        line = {
+            "metric": METRIC, "value": round(us_block, 2), "unit": "µs per draft block",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(step_ms, 5), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "L": w.L, "V": w.V, "d": w.d, "T": T,
+                       "conv_calls": w.conv_calls, "step": "tail + 20 conv (CUDA graph)",
+                       "l2": "flushed (256 MB write) before every timed step"},
+            "tail_us": round(res["tail"]["mean_ms"] * 1e3, 2),
+            "conv20_us": round(res["conv"]["mean_ms"] * 1e3 * w.conv_calls, 2),
+            "kernel_us": {k: round(res[k]["mean_ms"] * 1e3, 2) for k in
+                          ("topk", "select", "walk", "conv")},
+            "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
+            "per_kernel": res["per_kernel"],
+            "b64": batched,
+            "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": "µs per draft block",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": res["kernels_per_step"] * args.steps,
+            "kernels_per_step": res["kernels_per_step"],
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,173 @@
+/*
+ * dfl2: the DFlash 2 draft tail on one GB300 (sm_103a), as a C ABI.
+ *
+ * The tail runs once per draft-verify cycle, after the drafter's one-pass
+ * forward and before the target's verify pass:
+ *
+ *   logits U [B,L,V] --top-16--> candidates --pair scores S_t(a,b)--> walk --> draft tokens
+ *
+ * plus the two-tap dynamic conv that the drafter applies before and after each
+ * attention and feed-forward sublayer (5 layers x 4 insertion points).
+ *
+ * Sources (page title, section):
+ *   [SEL]  "DFlash 2: Keep Drafting Parallel" (papercache.org digest of the
+ *          Inco AI post), 方法细节 > 轻量级路径选择器 (Lightweight Path Selector):
+ *          top-16 candidates per position, the pair-score equation
+ *          S_t(a,b) = U_t(b) + <A(a) ⊙ H(h_t), B(b)>, and the walk over the
+ *          precomputed scores starting from the last verified token.
+ *   [CONV] same page, 方法细节 > 轻量级局部卷积 (Lightweight Local Convolution):
+ *          Conv_k(x)_t = k_{t,0} ⊙ x_t + k_{t,1} ⊙ x_{t-1}, a learned base
+ *          kernel plus a correction from the hidden state shared by every 16
+ *          channels, and position 0 reading the last verified token.
+ *   [TAB2] same page, Table 2 (+2.0M selector parameters) and the conv's
+ *          "+16.5M" paragraph; these fix A(a) = W_A E[a], B(b) = W_B E[b],
+ *          H(h) = sigmoid(W_H h) with W_* in R^{256 x d}, and a correction map
+ *          of 2 d/16 rows for both taps.
+ *   [WALK] "DFlash 2: The Drafter Stopped Guessing Alone" (rohitghumare.com),
+ *          "Selection beats correction": greedy follows the best successor;
+ *          sampling draws from the same scores.
+ *
+ * Conventions for every entry point:
+ *   - Tensor pointers are DEVICE memory owned by the caller, row-major and
+ *     contiguous, 16-byte aligned.  bf16 tensors are passed as uint16_t bit
+ *     patterns.  Nothing is allocated by the library; scratch memory is a
+ *     caller-provided workspace of at least *_workspace_size() bytes.
+ *   - Work is enqueued on the caller's stream; no call synchronises the host
+ *     (except dfl2_device_error, which says so).
+ *   - Arguments are validated on the host before anything is launched; a bad
+ *     argument returns a status and launches nothing.  Launch failures return
+ *     DFL2_ERR_CUDA.  No call throws, aborts or prints.  dfl2_last_error()
+ *     returns a thread-local message for the last failing call.
+ *   - Fixed method sizes: k = 16 candidates, r = 256 selector rank; d must be a
+ *     multiple of 64 for dfl2_select and of 16 for dfl2_conv2; V >= 16, L >= 1,
+ *     B >= 1.  Logits rows must be a whole number of 16-byte units (V % 8 == 0
+ *     for bf16, V % 4 == 0 for float32).
+ *   - Every wait inside a kernel is bounded; a wait that runs out records a
+ *     code in a per-device error word (dfl2_device_error) and the kernel
+ *     returns, leaving the context usable.
+ *   - Workspaces must be zero-filled once before their first use (for example
+ *     with dfl2_workspace_init); the library keeps them valid afterwards.
+ */
+#ifndef DFL2_H
+#define DFL2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st* dfl2_stream;
+
+typedef enum dfl2_status {
+  DFL2_OK = 0,
+  DFL2_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer, T < 0 ... */
+  DFL2_ERR_UNSUPPORTED = 2, /* k != 16, r != 256, d or V not of a supported multiple */
+  DFL2_ERR_WORKSPACE = 3,   /* workspace missing or smaller than *_workspace_size() */
+  DFL2_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  DFL2_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (see dfl2_device_error) */
+} dfl2_status;
+
+typedef enum dfl2_dtype { DFL2_F32 = 0, DFL2_BF16 = 1 } dfl2_dtype;
+
+/* Library version string, e.g. "dfl2 0.1 sm_103a". */
+const char* dfl2_version(void);
+
+/* Copies the calling thread's last error message (NUL-terminated, truncated to
+ * len) and returns its full length. */
+size_t dfl2_last_error(char* buf, size_t len);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t dfl2_launch_count(void);
+
+/* Zero-fills a workspace on the stream (one cudaMemsetAsync). */
+dfl2_status dfl2_workspace_init(void* ws, size_t ws_bytes, dfl2_stream stream);
+
+/* Reads, and if clear != 0 resets, the current device's error word.  0 means no
+ * kernel recorded a failed wait.  SYNCHRONISES the current device. */
+dfl2_status dfl2_device_error(uint32_t* code, int clear);
+
+/* ------------------------------------------------------------------ top-16
+ * [SEL] "每个位置提取并保留 Top-16": for each of the B*L rows of logits [B,L,V]
+ * (dtype float32 or bf16), the k = 16 largest logits, ordered by value
+ * descending and then index ascending (-0.0 ties +0.0; NaN is not supported).
+ * Writes cand_idx int32 [B,L,16] and cand_val float32 [B,L,16] (the logit,
+ * widened exactly; a zero is written as +0.0).  ws: dfl2_topk_workspace_size
+ * bytes (split-row partial lists and per-row tickets).
+ */
+size_t dfl2_topk_workspace_size(int B, int L, int V);
+dfl2_status dfl2_topk(const void* logits, dfl2_dtype dtype, int B, int L, int V, int k,
+                      int32_t* cand_idx, float* cand_val, void* ws, size_t ws_bytes,
+                      dfl2_stream stream);
+
+/* ------------------------------------------------------------------ pair scores
+ * [SEL equation], [TAB2] reading:
+ *   A(a) = W_A E[a], B(b) = W_B E[b], H(h_t) = sigmoid(W_H h_t)   (W_* [256,d], E [V,d])
+ *   S[b,t,i,j] = cand_val[b,t,j] + sum_q A_q(a_i) H_q(h_{b,t}) B_q(cand_idx[b,t,j])
+ * where a_i = cand_idx[b,t-1,i] for t >= 1, and for t = 0 only row i = 0 is
+ * defined, with a_0 = verified_tok[b] (rows 1..15 of t = 0 are -inf).
+ * hidden [B,L,d] bf16 is the drafter's final hidden state at each position.
+ * scores float32 [B,L,16,16]; projections accumulate in float32.
+ * ws: dfl2_select_workspace_size bytes (projected candidates and gates).
+ */
+size_t dfl2_select_workspace_size(int B, int L, int d);
+dfl2_status dfl2_select(const int32_t* cand_idx, const float* cand_val,
+                        const int32_t* verified_tok, const uint16_t* hidden, const uint16_t* E,
+                        const uint16_t* W_A, const uint16_t* W_B, const uint16_t* W_H, int B,
+                        int L, int V, int d, int r, float* scores, void* ws, size_t ws_bytes,
+                        dfl2_stream stream);
+
+/* ------------------------------------------------------------------ walk
+ * [SEL "全并行打分与低延迟路径步进"], [WALK].  One sequential pass per
+ * sequence over scores [B,L,16,16]: prev starts at row 0 of position 0 (the
+ * verified token); at each t the step reads row prev of S[b,t] and picks
+ *   temperature == 0: the lowest slot holding the row maximum (greedy);
+ *   temperature  > 0: p_j = exp((S_j - max)/T), Z = sum_j p_j, u uniform in
+ *                     [0,1), the first j with u Z < p_0 + ... + p_j.
+ * u = (w >> 8) * 2^-24, w = word 0 of Philox4x32-10 (Salmon et al., SC'11)
+ * with counter (t, lo32(cycle_offset), hi32(cycle_offset), 0) and key
+ * (lo32(seeds[b]), hi32(seeds[b])).  Then prev = j*.
+ * Writes tokens [B,L] = cand_idx[b,t,j*]; slots [B,L] = j* (nullable);
+ * q [B,L,16] = p/Z, the draft distribution the verifier's rejection sampling
+ * needs (one-hot when greedy; nullable).  seeds: device uint64 [B], may be NULL
+ * when temperature == 0.
+ */
+dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L,
+                      float temperature, const uint64_t* seeds, uint64_t cycle_offset,
+                      int32_t* tokens, int32_t* slots, float* q, dfl2_stream stream);
+
+/* ------------------------------------------------------------------ conv
+ * [CONV equation], [TAB2] reading.  G = d/16 correction groups.
+ *   corr[b,t,j,g] = sum_c W_c[j*G + g, c] x[b,t,c]          (j = tap 0, 1)
+ *   k_j[c]        = base[j,c] + corr[b,t,j,c/16]
+ *   y[b,t,c]      = k_0[c] x[b,t,c] + k_1[c] x[b,t-1,c],   x[b,-1,:] = x_prev[b,:]
+ * x, y [B,L,d] bf16; x_prev [B,d] bf16 (the verified token's representation
+ * at this insertion point); base float32 [2,d]; W_c bf16 [2G, d] with rows
+ * [tap-0 groups; tap-1 groups].  float32 arithmetic, y rounded once to bf16
+ * (nearest even).  y must not overlap x or x_prev.  No workspace.
+ */
+dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
+                       const uint16_t* W_c, int B, int L, int d, uint16_t* y,
+                       dfl2_stream stream);
+
+/* ------------------------------------------------------------------ fused tail
+ * top-16 -> pair scores -> walk in one call on one stream, with no host
+ * synchronisation: the same results as dfl2_topk, dfl2_select and dfl2_walk
+ * called in sequence.  cand_idx, cand_val, scores, slots and q are optional
+ * outputs (NULL: kept in the workspace / not written).
+ */
+size_t dfl2_tail_workspace_size(int B, int L, int V, int d);
+dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verified_tok,
+                      const uint16_t* hidden, const uint16_t* E, const uint16_t* W_A,
+                      const uint16_t* W_B, const uint16_t* W_H, int B, int L, int V, int d,
+                      float temperature, const uint64_t* seeds, uint64_t cycle_offset,
+                      int32_t* tokens, int32_t* slots, float* q, int32_t* cand_idx,
+                      float* cand_val, float* scores, void* ws, size_t ws_bytes,
+                      dfl2_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFL2_H */

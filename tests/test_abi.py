@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/dfl2.h declares, and rejects bad arguments on the host, before
+any CUDA call, with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import draft_selection_gb300 as dfl2
+from draft_selection_gb300 import build as dbuild
+
+HDR = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                   "dfl2.h")
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+A = 0x10000      # a 16-byte aligned stand-in address: never dereferenced by these tests
+A2 = 0x20000
+
+
+def declared_functions():
+    text = open(HDR).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dfl2_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dbuild.build()
+    return dfl2.load()
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_counters(lib):
+    assert dfl2.dfl2_version().startswith("dfl2")
+    assert dfl2.dfl2_launch_count() >= 0
+
+
+def test_topk_rejects_bad_arguments(lib):
+    ws = dfl2.dfl2_topk_workspace_size(1, 8, 1024)
+    assert ws > 0
+    f = lib.dfl2_topk
+    assert f(A, 1, 1, 8, 1024, 17, A, A, A, ws, None) == UNSUPPORTED      # k != 16
+    assert f(A, 7, 1, 8, 1024, 16, A, A, A, ws, None) == UNSUPPORTED      # dtype
+    assert f(A, 1, 1, 8, 1020, 16, A, A, A, ws, None) == UNSUPPORTED      # bf16 rows not 16 B
+    assert f(A, 0, 1, 8, 1022, 16, A, A, A, ws, None) == UNSUPPORTED      # f32 rows not 16 B
+    assert f(A, 1, 1, 8, 8, 16, A, A, A, ws, None) == INVALID             # V < 16
+    assert f(A, 1, 0, 8, 1024, 16, A, A, A, ws, None) == INVALID          # B = 0
+    assert f(A, 1, 1, 0, 1024, 16, A, A, A, ws, None) == INVALID          # L = 0
+    assert f(None, 1, 1, 8, 1024, 16, A, A, A, ws, None) == INVALID       # NULL logits
+    assert f(A + 2, 1, 1, 8, 1024, 16, A, A, A, ws, None) == INVALID      # misaligned
+    assert f(A, 1, 1, 8, 1024, 16, A, A, None, ws, None) == WORKSPACE     # no workspace
+    assert f(A, 1, 1, 8, 1024, 16, A, A, A, ws - 1, None) == WORKSPACE    # too small
+    assert "workspace" in dfl2.dfl2_last_error()
+
+
+def test_select_rejects_bad_arguments(lib):
+    ws = dfl2.dfl2_select_workspace_size(1, 8, 1024)
+    f = lib.dfl2_select
+    good = [A] * 8
+    assert f(*good, 1, 8, 32768, 1024, 255, A, A, ws, None) == UNSUPPORTED   # r != 256
+    assert f(*good, 1, 8, 32768, 1000, 256, A, A, ws, None) == UNSUPPORTED   # d % 64
+    assert f(*good, 1, 8, 8, 1024, 256, A, A, ws, None) == INVALID           # V < 16
+    bad = list(good)
+    bad[4] = None                                                             # NULL E
+    assert f(*bad, 1, 8, 32768, 1024, 256, A, A, ws, None) == INVALID
+    assert "E is NULL" in dfl2.dfl2_last_error()
+    assert f(*good, 1, 8, 32768, 1024, 256, A, A, 16, None) == WORKSPACE
+
+
+def test_walk_rejects_bad_arguments(lib):
+    f = lib.dfl2_walk
+    assert f(A, A, 1, 8, -1.0, A, 0, A, None, None, None) == INVALID          # T < 0
+    assert f(A, A, 1, 8, float("nan"), A, 0, A, None, None, None) == INVALID  # T NaN
+    assert f(A, A, 1, 8, float("inf"), A, 0, A, None, None, None) == INVALID  # T inf
+    assert f(A, A, 1, 8, 1.0, None, 0, A, None, None, None) == INVALID        # no seeds
+    assert f(A, A, 1, 8, 1.0, A, 0, None, None, None, None) == INVALID        # no tokens
+    assert f(A, A, 1, 8, 1.0, A, 0, A, A + 4, None, None) == INVALID          # misaligned slots
+    assert f(A, A, 0, 8, 0.0, None, 0, A, None, None, None) == INVALID        # B = 0
+
+
+def test_conv_rejects_bad_arguments(lib):
+    f = lib.dfl2_conv2
+    assert f(A, A2, A, A, 1, 8, 1000, A2 + 0x100000, None) == UNSUPPORTED     # d % 16
+    assert f(A, A2, A, A, 1, 8, 8, A2 + 0x100000, None) == UNSUPPORTED        # d < 16
+    assert f(None, A2, A, A, 1, 8, 1024, A2 + 0x100000, None) == INVALID      # NULL x
+    assert f(A, A2, A, A, 1, 8, 1024, A + 16, None) == INVALID                # y overlaps x
+    assert "overlaps" in dfl2.dfl2_last_error()
+    assert f(A, A2, A, A, 1, 0, 1024, A2 + 0x100000, None) == INVALID         # L = 0
+
+
+def test_tail_rejects_bad_arguments(lib):
+    ws = dfl2.dfl2_tail_workspace_size(1, 16, 151936, 2560)
+    assert ws >= dfl2.dfl2_topk_workspace_size(1, 16, 151936) + dfl2.dfl2_select_workspace_size(
+        1, 16, 2560)
+    f = lib.dfl2_tail
+    args = lambda **kw: [kw.get("logits", A), kw.get("dtype", 1), A, A, A, A, A, A, 1, 16,
+                         kw.get("V", 151936), kw.get("d", 2560), kw.get("T", 1.0),
+                         kw.get("seeds", A), 0, A, None, None, None, None, None, A,
+                         kw.get("ws", ws), None]
+    assert f(*args(T=-0.5)) == INVALID
+    assert f(*args(seeds=None)) == INVALID
+    st = f(*args(seeds=None, T=0.0))   # greedy needs no seeds: whatever fails next, not that
+    assert st != OK and "seeds" not in dfl2.dfl2_last_error()
+    assert f(*args(d=2500)) == UNSUPPORTED
+    assert f(*args(V=151930)) == UNSUPPORTED
+    assert f(*args(ws=ws - 256)) == WORKSPACE
+
+
+def test_workspace_sizes_are_monotone(lib):
+    a = dfl2.dfl2_tail_workspace_size(1, 8, 32768, 1024)
+    b = dfl2.dfl2_tail_workspace_size(64, 16, 151936, 2560)
+    c = dfl2.dfl2_tail_workspace_size(256, 16, 262144, 6144)
+    assert 0 < a < b < c
+    assert dfl2.dfl2_topk_workspace_size(0, 8, 1024) == 0
+
+
+def test_python_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(dbuild, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(dfl2, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        dfl2.load()

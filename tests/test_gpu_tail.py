@@ -1,0 +1,120 @@
+"""GPU parity of the fused tail (top-16 -> pair scores -> walk in one call)
+against the oracle run step by step, on every workload shape.
+
+Candidates: bit-exact.  Scores: 1e-3 relative.  Walk: step-wise replay
+against the oracle's own double-precision scores, given the GPU's previous
+choice; steps inside the greedy margin / sampling boundary are counted."""
+import numpy as np
+import pytest
+import torch
+
+import draft_selection_gb300 as dfl2
+from draft_selection_gb300 import workloads as wl
+import oracle
+from _parity import assert_scores_close, replay_walk, report
+from test_gpu_select import oracle_select_subset
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from draft_selection_gb300 import build
+    build.build()
+    dfl2.load()
+
+
+def run_tail(w, lg, inp, T, seeds, cycle=0):
+    B, L, V, d = w.B, w.L, w.V, w.d
+    out = dict(
+        tokens=torch.empty(B, L, dtype=torch.int32, device="cuda"),
+        slots=torch.empty(B, L, dtype=torch.int32, device="cuda"),
+        q=torch.empty(B, L, 16, dtype=torch.float32, device="cuda"),
+        cand_idx=torch.empty(B, L, 16, dtype=torch.int32, device="cuda"),
+        cand_val=torch.empty(B, L, 16, dtype=torch.float32, device="cuda"),
+        scores=torch.empty(B, L, 16, 16, dtype=torch.float32, device="cuda"),
+    )
+    ws = dfl2.workspace(dfl2.dfl2_tail_workspace_size(B, L, V, d))
+    sd = torch.from_numpy(seeds.view(np.int64)).cuda()
+    c = lambda t: t if t.is_cuda else t.cuda()
+    dfl2.dfl2_tail(c(lg), c(inp["verified"]), c(inp["hidden"]), c(inp["E"]), c(inp["W_A"]),
+                   c(inp["W_B"]), c(inp["W_H"]), T, sd, cycle, out["tokens"], ws,
+                   slots=out["slots"], q=out["q"], cand_idx=out["cand_idx"],
+                   cand_val=out["cand_val"], scores=out["scores"])
+    torch.cuda.synchronize()
+    assert dfl2.dfl2_device_error() == 0
+    return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def check_tail(w, lg, inp, T, seeds, cycle, seqs):
+    g = run_tail(w, lg, inp, T, seeds, cycle)
+    V = w.V
+    flat = lg.reshape(w.rows, V)
+    rows = [b * w.L + t for b in seqs for t in range(w.L)]
+    ri, rv = oracle.topk(wl.host(flat[rows]), 16)
+    np.testing.assert_array_equal(g["cand_idx"][seqs].reshape(-1, 16), ri)
+    np.testing.assert_array_equal(g["cand_val"][seqs].reshape(-1, 16), rv)
+    ci = torch.from_numpy(g["cand_idx"])
+    cv = torch.from_numpy(g["cand_val"])
+    ref = oracle_select_subset(ci, cv, inp["verified"].cpu(), inp, seqs)
+    worst = assert_scores_close(g["scores"][seqs], ref, w.name)
+    allowed = replay_walk(ref, g["slots"][seqs], T, seeds[seqs], cycle, what=f"{w.name} T={T}")
+    np.testing.assert_array_equal(
+        g["tokens"], np.take_along_axis(g["cand_idx"], g["slots"][..., None].astype(np.int64),
+                                        2)[..., 0])
+    report(kind="tail", what=f"{w.name} T={T}", seqs=len(seqs), worst_err_over_tol=worst,
+           allowed_walk_mismatches=allowed)
+    return g
+
+
+@pytest.mark.parametrize("name,T,e_std", [
+    ("tiny_l8_v32k", 0.0, 0.02), ("tiny_l8_v32k", 0.0, 1.0),
+    ("drafter4b_l16", 0.0, 0.02), ("drafter4b_l16", 1.0, 0.02), ("drafter4b_l16", 1.0, 1.0),
+    ("drafter27b_l8", 0.0, 0.02), ("drafter27b_l8", 0.0, 1.0),
+])
+def test_small_workloads(name, T, e_std):
+    w = wl.WORKLOADS[name].with_(e_std=e_std)
+    lg = wl.make_logits(w, "cpu")
+    inp = wl.make_tail_inputs(w, "cpu")
+    check_tail(w, lg, inp, T, inp["seeds"], 0, list(range(w.B)))
+
+
+@pytest.mark.parametrize("name,T,nseq", [("serving_b64", 1.0, 3), ("stress_b256_ties", 0.0, 2),
+                                         ("stress_b256_ties", 0.7, 2)])
+def test_batched_workloads_sampled(name, T, nseq):
+    w = wl.WORKLOADS[name]
+    lg = wl.make_logits(w, "cuda")
+    inp = wl.make_tail_inputs(w, "cuda")
+    seqs = sorted({0, w.B - 1} | set(np.random.default_rng(5).choice(w.B, nseq, False).tolist()))
+    check_tail(w, lg, inp, T, inp["seeds"], 12345, seqs)
+
+
+def test_tail_equals_the_three_calls():
+    """The fused call gives exactly what dfl2_topk, dfl2_select and dfl2_walk give."""
+    w = wl.WORKLOADS["drafter4b_l16"].with_(B=3, e_std=1.0)
+    lg = wl.make_logits(w, "cpu").cuda()
+    inp = {k: (v.cuda() if isinstance(v, torch.Tensor) else v)
+           for k, v in wl.make_tail_inputs(w, "cpu").items()}
+    g = run_tail(w, lg, inp, 1.0, inp["seeds"], 77)
+    B, L, V, d = w.B, w.L, w.V, w.d
+    idx = torch.empty(B, L, 16, dtype=torch.int32, device="cuda")
+    val = torch.empty(B, L, 16, dtype=torch.float32, device="cuda")
+    dfl2.dfl2_topk(lg, idx, val, dfl2.workspace(dfl2.dfl2_topk_workspace_size(B, L, V)))
+    S = torch.empty(B, L, 16, 16, device="cuda")
+    dfl2.dfl2_select(idx, val, inp["verified"], inp["hidden"], inp["E"], inp["W_A"], inp["W_B"],
+                     inp["W_H"], S, dfl2.workspace(dfl2.dfl2_select_workspace_size(B, L, d)))
+    tok = torch.empty(B, L, dtype=torch.int32, device="cuda")
+    sd = torch.from_numpy(inp["seeds"].view(np.int64)).cuda()
+    dfl2.dfl2_walk(S, idx, 1.0, sd, 77, tok)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(idx.cpu().numpy(), g["cand_idx"])
+    np.testing.assert_array_equal(S.cpu().numpy(), g["scores"])
+    np.testing.assert_array_equal(tok.cpu().numpy(), g["tokens"])
+
+
+def test_minimal_block():
+    w = wl.WORKLOADS["tiny_l8_v32k"].with_(L=1, V=16, d=64, e_std=1.0)
+    lg = wl.make_logits(w, "cpu")
+    inp = wl.make_tail_inputs(w, "cpu")
+    check_tail(w, lg, inp, 0.0, inp["seeds"], 0, [0])

@@ -1,0 +1,155 @@
+"""GPU parity of the top-16 step against the oracle's full sort, through the C ABI.
+
+Bit-exact: indices and values, with ties broken by value descending then index
+ascending.  Small workloads are compared on every row; the batched workloads
+on sampled rows against the oracle and on every row through properties that
+hold at any size."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import draft_selection_gb300 as dfl2
+from draft_selection_gb300 import workloads as wl
+import oracle
+
+pytestmark = pytest.mark.gpu
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from draft_selection_gb300 import build
+    build.build()
+    dfl2.load()
+
+
+def gpu_topk(logits: torch.Tensor):
+    B, L, V = logits.shape
+    idx = torch.empty(B, L, 16, dtype=torch.int32, device="cuda")
+    val = torch.empty(B, L, 16, dtype=torch.float32, device="cuda")
+    ws = dfl2.workspace(dfl2.dfl2_topk_workspace_size(B, L, V))
+    dfl2.dfl2_topk(logits, idx, val, ws)
+    torch.cuda.synchronize()
+    assert dfl2.dfl2_device_error() == 0
+    return idx.cpu().numpy(), val.cpu().numpy()
+
+
+def check_rows(logits: torch.Tensor, idx, val, rows=None):
+    host = wl.host(logits)
+    V = host.shape[-1]
+    flat = host.reshape(-1, V)
+    gi, gv = idx.reshape(-1, 16), val.reshape(-1, 16)
+    rows = range(flat.shape[0]) if rows is None else rows
+    sel = np.array(list(rows))
+    ri, rv = oracle.topk(flat[sel], 16)
+    np.testing.assert_array_equal(gi[sel], ri)
+    np.testing.assert_array_equal(gv[sel], rv)
+
+
+def check_properties(logits: torch.Tensor, idx: np.ndarray, val: np.ndarray):
+    """At any size: values are the 16 largest (torch.topk's multiset, sorted),
+    each index holds its value, and the members tied with the 16th value are the
+    lowest-index elements of that value."""
+    R = idx.shape[0] * idx.shape[1]
+    V = logits.shape[-1]
+    lg = logits.reshape(R, V)
+    gi = torch.from_numpy(idx.reshape(R, 16)).cuda().long()
+    gv = torch.from_numpy(val.reshape(R, 16)).cuda()
+    for r0 in range(0, R, 256):
+        x = lg[r0:r0 + 256].float()
+        i, v = gi[r0:r0 + 256], gv[r0:r0 + 256]
+        tv = torch.topk(x, 16, dim=1, sorted=True).values
+        assert torch.equal(tv, v), "values differ from the 16 largest"
+        assert torch.equal(torch.gather(x, 1, i), v), "an index does not hold its value"
+        v16 = v[:, 15:16]
+        n_gt = (x > v16).sum(1)
+        members_eq = (v == v16).sum(1)
+        assert torch.all(n_gt + members_eq == 16)
+        # the tied members must be the first `members_eq` positions holding v16
+        eq = (x == v16)
+        rank = torch.cumsum(eq.int(), dim=1)
+        first_ok = torch.gather(rank, 1, i) <= members_eq[:, None]
+        assert torch.all(first_ok | (v != v16)), "tie-break is not index ascending"
+        assert torch.all(i[:, 1:] != i[:, :-1])
+
+
+def test_golden_ties_case():
+    g = json.load(open(os.path.join(GOLD, "topk_ties.json")))
+    row = np.array([float(x) for x in g["logits"]], np.float32)
+    for dt in (torch.float32, torch.bfloat16):
+        lg = torch.tensor(row).to(dt).view(1, 1, -1).cuda()
+        idx, val = gpu_topk(lg)
+        assert idx[0, 0].tolist() == g["idx"]
+        assert val[0, 0].tolist() == g["val"]
+
+
+@pytest.mark.parametrize("name", ["tiny_l8_v32k", "drafter4b_l16", "drafter27b_l8"])
+def test_small_workloads_all_rows(name):
+    w = wl.WORKLOADS[name]
+    lg = wl.make_logits(w, "cpu").cuda()
+    idx, val = gpu_topk(lg)
+    check_rows(lg, idx, val)
+
+
+def test_serving_b64_sampled_rows_and_properties():
+    w = wl.WORKLOADS["serving_b64"]
+    lg = wl.make_logits(w, "cuda")
+    idx, val = gpu_topk(lg)
+    check_properties(lg, idx, val)
+    rng = np.random.default_rng(0)
+    rows = sorted(set(rng.choice(w.rows, 24, replace=False).tolist()) | {0, w.rows - 1})
+    sub = lg.reshape(w.rows, w.V)[rows].reshape(1, len(rows), w.V)
+    check_rows(sub, idx.reshape(-1, 16)[rows].reshape(1, -1, 16),
+               val.reshape(-1, 16)[rows].reshape(1, -1, 16))
+
+
+def test_stress_ties_sampled_rows_and_properties():
+    w = wl.WORKLOADS["stress_b256_ties"]
+    lg = wl.make_logits(w, "cuda")
+    idx, val = gpu_topk(lg)
+    check_properties(lg, idx, val)
+    rng = np.random.default_rng(1)
+    rows = sorted(set(rng.choice(w.rows, 12, replace=False).tolist()) | {0, w.rows - 1})
+    sub = lg.reshape(w.rows, w.V)[rows].reshape(1, len(rows), w.V)
+    check_rows(sub, idx.reshape(-1, 16)[rows].reshape(1, -1, 16),
+               val.reshape(-1, 16)[rows].reshape(1, -1, 16))
+    # the quantised logits must actually produce ties at the 16th place
+    v = val.reshape(-1, 16)
+    assert np.mean(v[:, 14] == v[:, 15]) > 0.5
+
+
+@pytest.mark.parametrize("B,L,V,dt", [
+    (1, 1, 16, torch.float32),       # minimum vocabulary, one row
+    (1, 1, 16, torch.bfloat16),
+    (1, 3, 24, torch.float32),       # less than one 16-byte vector past the minimum
+    (2, 3, 8200, torch.bfloat16),    # two full 8 KB tiles plus a 16-byte ragged tile
+    (1, 5, 12292, torch.float32),    # ragged last tile, float32
+    (37, 3, 1000, torch.bfloat16),   # many short rows: several rows per CTA
+    (3, 7, 65536 + 8, torch.bfloat16),
+])
+def test_edge_shapes(B, L, V, dt):
+    g = torch.Generator().manual_seed(B * 1000 + L * 10 + V)
+    lg = (torch.randn(B, L, V, generator=g) * 3).to(dt)
+    idx, val = gpu_topk(lg.cuda())
+    check_rows(lg, idx, val)
+
+
+def test_degenerate_rows():
+    V = 4096
+    rows = []
+    rows.append(torch.zeros(V))                                   # all equal: indices 0..15
+    r = torch.full((V,), float("-inf")); r[100] = 1.0; rows.append(r)   # mostly -inf
+    r = torch.zeros(V); r[::2] = -0.0; rows.append(r)             # signed zeros tie
+    r = torch.arange(V, dtype=torch.float32); rows.append(r)      # best at the very end
+    r = -torch.arange(V, dtype=torch.float32); rows.append(r)     # best at the start
+    r = torch.full((V,), 5.0); r[-16:] = 6.0; rows.append(r)      # winners in the last vector
+    lg = torch.stack(rows).view(1, len(rows), V)
+    for dt in (torch.float32, torch.bfloat16):
+        x = lg.to(dt)
+        idx, val = gpu_topk(x.cuda())
+        check_rows(x, idx, val)
+    assert idx[0, 0].tolist() == list(range(16))
