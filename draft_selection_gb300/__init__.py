@@ -54,6 +54,8 @@ def load():
     L.dfl2_topk_workspace_size.argtypes = [I, I, I]
     L.dfl2_topk_workspace_size.restype = SZ
     L.dfl2_topk.argtypes = [P, I, I, I, I, I, P, P, P, SZ, P]
+    L.dfl2_topk_noalloc.argtypes = [P, I, I, I, I, I, P, P, P]
+    L.dfl2_topk_noalloc.restype = I
     L.dfl2_select_workspace_size.argtypes = [I, I, I]
     L.dfl2_select_workspace_size.restype = SZ
     L.dfl2_select.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]
@@ -157,6 +159,16 @@ def dfl2_topk(logits, cand_idx, cand_val, ws, k: int = NCAND, stream=None, *, di
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check(load().dfl2_topk(_ptr(logits), dt, B, L, V, k, _ptr(cand_idx), _ptr(cand_val),
                             _ptr(ws), wb, _stream(stream)))
+
+
+def dfl2_topk_noalloc(logits, cand_idx, cand_val, k: int = NCAND, stream=None, *, dims=None,
+                      dtype=None) -> None:
+    """dfl2_topk without a workspace, for callers that cannot allocate device
+    memory: the library's own fixed scratch array is used instead."""
+    B, L, V = dims if dims is not None else logits.shape
+    dt = dtype if dtype is not None else _dtype_code(logits)
+    _check(load().dfl2_topk_noalloc(_ptr(logits), dt, B, L, V, k, _ptr(cand_idx), _ptr(cand_val),
+                                    _stream(stream)))
 
 
 def dfl2_select(cand_idx, cand_val, verified_tok, hidden, E, W_A, W_B, W_H, scores, ws,

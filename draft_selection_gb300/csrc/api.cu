@@ -204,6 +204,22 @@ namespace dfl2 {
 void count_launch(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
 DeviceInfo device_info() { return g_dev[g_cur_dev].info; }
 uint32_t* device_error_word() { return g_dev[g_cur_dev].err; }
+
+// The checks of dfl2_topk apart from the workspace, for entry points that live
+// in other translation units: first those that need no CUDA call, then the
+// device ones (which also set up this device's cached state).
+dfl2_status check_topk_host(const void* logits, int dtype, int B, int L, int V, int k,
+                            const void* cand_idx, const void* cand_val) {
+  DFL2_TRY(check_topk_args(dtype, B, L, V, k));
+  return check_host({{logits, "logits"}, {cand_idx, "cand_idx"}, {cand_val, "cand_val"}});
+}
+dfl2_status check_topk_device(const void* logits, const void* cand_idx, const void* cand_val) {
+  DFL2_TRY(ensure_device());
+  return check_device({{logits, "logits"}, {cand_idx, "cand_idx"}, {cand_val, "cand_val"}});
+}
+// Records the calling thread's error message; returns st.
+dfl2_status report_error(dfl2_status st, const char* msg) { return fail(st, "%s", msg); }
+dfl2_status report_cuda_error(cudaError_t e, const char* what) { return cuda_fail(e, what); }
 }  // namespace dfl2
 
 extern "C" {

@@ -102,6 +102,22 @@ dfl2_status dfl2_topk(const void* logits, dfl2_dtype dtype, int B, int L, int V,
                       int32_t* cand_idx, float* cand_val, void* ws, size_t ws_bytes,
                       dfl2_stream stream);
 
+/* ------------------------------------------------------------------ top-16, no allocation
+ * No counterpart on the pages: a convenience of this library.  The same result
+ * as dfl2_topk, for callers that cannot allocate device memory, such as serving
+ * engines that reserve the GPU's memory for their own pool at start-up and
+ * forbid later cudaMalloc, or plug-ins that get only input and output pointers.
+ * The scratch dfl2_topk keeps in its workspace lives instead in a fixed 4 MiB
+ * array of library-owned device memory (held on every GPU that loads the
+ * library until the process exits); problems whose dfl2_topk_workspace_size
+ * exceeds 4 MiB return DFL2_ERR_WORKSPACE without launching.  The first call on
+ * a device looks up that array's address; make it before any stream capture.
+ * All calls share the array, so calls whose kernels overlap on the GPU (other
+ * streams or threads) race; calls in order on one stream are safe.
+ */
+dfl2_status dfl2_topk_noalloc(const void* logits, dfl2_dtype dtype, int B, int L, int V, int k,
+                              int32_t* cand_idx, float* cand_val, dfl2_stream stream);
+
 /* ------------------------------------------------------------------ pair scores
  * [SEL equation], [TAB2] reading:
  *   A(a) = W_A E[a], B(b) = W_B E[b], H(h_t) = sigmoid(W_H h_t)   (W_* [256,d], E [V,d])
