@@ -143,6 +143,12 @@ dfl2_status check_shape(int B, int L) {
   return DFL2_OK;
 }
 
+// The walk keeps a sequence's L x 16 x 16 score table in shared memory.
+dfl2_status check_block_len(int L) {
+  if (L > 128) return fail(DFL2_ERR_UNSUPPORTED, "L=%d: draft blocks of at most 128 positions", L);
+  return DFL2_OK;
+}
+
 dfl2_status check_topk_args(int dtype, int B, int L, int V, int k) {
   DFL2_TRY(check_shape(B, L));
   if (dtype != DFL2_F32 && dtype != DFL2_BF16)
@@ -305,7 +311,7 @@ dfl2_status dfl2_select(const int32_t* cand_idx, const float* cand_val,
   DFL2_TRY(check_device(ptrs));
   DFL2_TRY(check_device_ptr(ws, "workspace"));
   cudaError_t e = dfl2::launch_select(plan, cand_idx, cand_val, verified_tok, bf(hidden), bf(E),
-                                      bf(W_A), bf(W_B), bf(W_H), V, scores, ws,
+                                      bf(W_A), bf(W_B), bf(W_H), V, scores, nullptr, ws,
                                       reinterpret_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return cuda_fail(e, "selector launch");
   return DFL2_OK;
@@ -315,6 +321,7 @@ dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L
                       float temperature, const uint64_t* seeds, uint64_t cycle_offset,
                       int32_t* tokens, int32_t* slots, float* q, dfl2_stream stream) {
   DFL2_TRY(check_shape(B, L));
+  DFL2_TRY(check_block_len(L));
   DFL2_TRY(check_temperature(temperature));
   const Ptrs ptrs = {{scores, "scores"}, {cand_idx, "cand_idx"}, {tokens, "tokens"},
                      {slots, "slots", true}, {q, "q", true},
@@ -363,6 +370,7 @@ dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verif
                       dfl2_stream stream) {
   DFL2_TRY(check_topk_args(dtype, B, L, V, dfl2::kCand));
   DFL2_TRY(check_select_args(B, L, V, d, dfl2::kRank));
+  DFL2_TRY(check_block_len(L));
   DFL2_TRY(check_temperature(temperature));
   const int es = dtype == DFL2_F32 ? 4 : 2;
   const TailLayout t = tail_layout(B, L, V, d, es);
@@ -383,11 +391,10 @@ dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verif
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dfl2::launch_topk(t.topk, logits, idx, val, w + t.topk_off, s, false);
   if (e != cudaSuccess) return cuda_fail(e, "top-16 launch");
+  const dfl2::WalkFuse wf{temperature, seeds, cycle_offset, tokens, slots, q};
   e = dfl2::launch_select(t.sel, idx, val, verified_tok, bf(hidden), bf(E), bf(W_A), bf(W_B),
-                          bf(W_H), V, S, w + t.sel_off, s, true);
-  if (e != cudaSuccess) return cuda_fail(e, "selector launch");
-  e = dfl2::launch_walk(S, idx, B, L, temperature, seeds, cycle_offset, tokens, slots, q, s, true);
-  if (e != cudaSuccess) return cuda_fail(e, "walk launch");
+                          bf(W_H), V, S, &wf, w + t.sel_off, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "selector + walk launch");
   return DFL2_OK;
 }
 

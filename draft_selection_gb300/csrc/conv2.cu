@@ -27,6 +27,7 @@ struct ConvArgs {
   __nv_bfloat16* y;
   int L, d, G;
   int TL, NG;
+  uint32_t* err;
 };
 
 __device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
@@ -47,22 +48,32 @@ __global__ void __launch_bounds__(kConvThreads) conv2_fma_kernel(ConvArgs a) {
   const int tl = min(TL, a.L - t0);  // positions in this tile
   const int ng = min(NG, G - g0);    // groups in this CTA
   const int rows = 2 * NG;           // W_c rows (both taps), some unused when ng < NG
-  // layout: xs [(TL+1) rows][d] bf16 | red [kConvWarps][rows][TL] f32 | corr [rows][TL] f32
+  // layout: xs [(TL+1) rows][d] bf16 | red [kConvWarps][rows][TL] f32 | corr [rows][TL] f32 | bar
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
   float* red = reinterpret_cast<float*>(smem + size_t(TL + 1) * d * 2);
   float* corr = red + kConvWarps * rows * TL;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(corr + rows * TL);
 
-  pdl_wait();
-  // Stage x_{t0-1} (x_prev at t0 == 0) and x_{t0..t0+tl-1}.
-  const int vec_per_row = d / 8;
-  for (int e = threadIdx.x; e < (tl + 1) * vec_per_row; e += kConvThreads) {
-    const int r = e / vec_per_row, v = e % vec_per_row;
-    const int t = t0 - 1 + r;
-    const __nv_bfloat16* src = t < 0 ? a.x_prev + size_t(b) * d
-                                     : a.x + (size_t(b) * a.L + t) * d;
-    reinterpret_cast<uint4*>(xs + size_t(r) * d)[v] = reinterpret_cast<const uint4*>(src)[v];
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
   __syncthreads();
+  pdl_wait();
+  // Stage x_{t0-1} (x_prev at t0 == 0) and x_{t0..t0+tl-1} with bulk copies:
+  // the rows are contiguous in x, apart from x_prev.
+  const int vec_per_row = d / 8;
+  if (threadIdx.x == 0) {
+    const uint32_t row_bytes = static_cast<uint32_t>(d) * 2;
+    mbar_arrive_expect_tx(bar, row_bytes * (tl + 1));
+    if (t0 == 0) {
+      bulk_g2s(xs, a.x_prev + size_t(b) * d, row_bytes, bar);
+      bulk_g2s(xs + d, a.x + size_t(b) * a.L * d, row_bytes * tl, bar);
+    } else {
+      bulk_g2s(xs, a.x + (size_t(b) * a.L + t0 - 1) * d, row_bytes * (tl + 1), bar);
+    }
+  }
+  if (!mbar_wait(bar, 0)) record_error(a.err, kDevErrConv);
 
   // Corrections: warps split the rows; with fewer rows than warps they also split K.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,6 +92,7 @@ __global__ void __launch_bounds__(kConvThreads) conv2_fma_kernel(ConvArgs a) {
       const uint4* wrow = reinterpret_cast<const uint4*>(a.W_c + (size_t(tap) * G + g0 + gl) * d);
       const int v_lo = kpart * kchunk;
       const int v_hi = min(vec_per_row, v_lo + kchunk);
+#pragma unroll 4
       for (int v = v_lo + lane; v < v_hi; v += 32) {
         const uint4 w = __ldg(wrow + v);
 #pragma unroll
@@ -121,7 +133,7 @@ __global__ void __launch_bounds__(kConvThreads) conv2_fma_kernel(ConvArgs a) {
 }
 
 size_t conv_smem_bytes(int TL, int NG, int d) {
-  return size_t(TL + 1) * d * 2 + size_t(kConvWarps + 1) * 2 * NG * TL * sizeof(float);
+  return size_t(TL + 1) * d * 2 + size_t(kConvWarps + 1) * 2 * NG * TL * sizeof(float) + 16;
 }
 
 bool g_conv_attr_set[64];
@@ -147,7 +159,7 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   const int sms = device_info().sms;
   int NG = kMaxNG;
   while (NG > 1 && (long long)((G + NG - 1) / NG) * tiles * B < 2LL * sms) NG >>= 1;
-  ConvArgs a{x, x_prev, base, W_c, y, L, d, G, TL, NG};
+  ConvArgs a{x, x_prev, base, W_c, y, L, d, G, TL, NG, device_error_word()};
   const dim3 grid((G + NG - 1) / NG, tiles, B);
   return launch_k(conv2_fma_kernel, grid, dim3(kConvThreads), conv_smem_bytes(TL, NG, d), s,
                   false, a);

@@ -137,17 +137,36 @@ cudaError_t launch_topk(const TopkPlan& p, const void* logits, int32_t* idx, flo
 // ---- projections + pair scores ---------------------------------------------
 struct SelectPlan {
   int B, L, d;
-  int M;               // B*(16L+1) candidate rows (verified token first, then 16 per position)
-  size_t P_off;        // float32 [M][512]: A(.) in columns 0..255, B(.) in 256..511
-  size_t H_off;        // float32 [B*L][256]
+  int MA;              // rows needing A(.): per sequence the verified token + 16 (L-1) candidates
+  int MB;              // rows needing B(.): per sequence 16 L candidates
+  int MH;              // hidden rows: B L
+  int M;               // MA (kept for reporting)
+  int kblocks;         // d / 64
+  int kps, splits;     // K blocks per split; K splits = CTAs of one cluster (reduced on chip)
+  size_t PA_off;       // float32 [MA][256]
+  size_t PB_off;       // float32 [MB][256]
+  size_t GH_off;       // float32 [MH][256], before the sigmoid
+  size_t ticket_off;   // uint32 [B]: per-sequence tickets of the fused pair + walk kernel
+  size_t choice_off;   // int32 [B*L][16]: per-row walk choice
+  size_t q_off;        // float32 [B*L][16][16]: per-row draft distribution
   size_t ws_bytes;
 };
 SelectPlan select_plan(int B, int L, int d);
+// The walk, when it runs inside the pair kernel (the fused tail).
+struct WalkFuse {
+  float T;
+  const uint64_t* seeds;
+  uint64_t cycle;
+  int32_t* tokens;
+  int32_t* slots;  // nullable
+  float* q;        // nullable
+};
 cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
                           const int32_t* verified, const __nv_bfloat16* hidden,
                           const __nv_bfloat16* E, const __nv_bfloat16* W_A,
                           const __nv_bfloat16* W_B, const __nv_bfloat16* W_H, int V,
-                          float* scores, void* ws, cudaStream_t s, bool pdl);
+                          float* scores, const WalkFuse* walk, void* ws, cudaStream_t s,
+                          bool pdl);
 
 // ---- walk ---------------------------------------------------------------------
 cudaError_t launch_walk(const float* scores, const int32_t* cand_idx, int B, int L, float T,
@@ -162,24 +181,275 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
 // ---- helpers ------------------------------------------------------------------
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Launch with optional programmatic-dependent-launch attribute.
+// Launch with optional programmatic-dependent-launch attribute and an optional
+// thread-block cluster of `cluster` CTAs along x.
 template <typename Kernel, typename... Args>
-cudaError_t launch_k(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
-                     Args... args) {
+cudaError_t launch_kc(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                      int cluster, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int n = 0;
   if (pdl) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
   }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = n ? attr : nullptr;
+  cfg.numAttrs = n;
   count_launch();
   return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+template <typename Kernel, typename... Args>
+cudaError_t launch_k(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                     Args... args) {
+  return launch_kc(kernel, grid, block, smem, s, pdl, 1, args...);
+}
+
+}  // namespace dfl2
+
+// ============================================================================
+// Blackwell tensor-core helpers (tcgen05, TMEM, TMA tensor maps), sm_100+.
+// ============================================================================
+namespace dfl2 {
+
+// ---- cp.async (16 B, L2 only) with zero fill, and proxy fence -------------
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Makes this thread's generic-proxy shared-memory writes (st.shared, cp.async)
+// visible to the async proxy (tensor cores, TMA).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---- TMA tiled 2D load -------------------------------------------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---- TMEM allocation (one warp, .sync.aligned) -------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* smem_dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(smem_dst)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---- UMMA descriptors ------------------------------------------------------------
+// Shared-memory matrix descriptor, K-major operand in the 128-byte swizzle
+// layout: rows of 64 bf16 (128 B), 8-row atoms of 1024 B (stride byte offset),
+// descriptor version 1, layout type 2 (SWIZZLE_128B).
+__device__ __forceinline__ uint64_t umma_desc_sw128(const void* smem_tile) {
+  const uint64_t addr = smem_u32(smem_tile);
+  uint64_t d = 0;
+  d |= (addr >> 4) & 0x3FFFull;          // start address
+  d |= uint64_t(1) << 16;                // leading byte offset (unused for swizzled K-major)
+  d |= uint64_t(1024 >> 4) << 32;        // stride byte offset: next 8-row atom
+  d |= uint64_t(1) << 46;                // descriptor version (sm_100)
+  d |= uint64_t(2) << 61;                // SWIZZLE_128B
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
+  return (1u << 4)                 // D format: f32
+         | (1u << 7)               // A format: bf16
+         | (1u << 10)              // B format: bf16
+         | (uint32_t(N >> 3) << 17)
+         | (uint32_t(M >> 4) << 24);
+}
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on bar when all previously issued tcgen05.mma of this thread complete.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+// 32 lanes x 32 consecutive fp32 columns: thread i of the warp gets lane (base+i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---- thread-block clusters (distributed shared memory) -----------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Shared-memory address of the same variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Host: 2D bf16 tensor map over a row-major [rows, cols] matrix, box
+// {64 cols, box_rows rows}, 128-byte swizzle.  Cached per (pointer, shape).
+// Returns false if the driver entry point is unavailable or encoding fails.
+bool tensor_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     void* out128);
+
+}  // namespace dfl2
+
+// ============================================================================
+// The walk's per-row decision ("DFlash 2: Keep Drafting Parallel", 方法细节 >
+// 轻量级路径选择器, "全并行打分与低延迟路径步进").  The step-t draw does not
+// depend on the path (its Philox counter is t), so the decision for every row
+// of every position can be made in parallel; the walk itself then only follows
+// the chosen slots from the verified token.
+// ============================================================================
+namespace dfl2 {
+
+// Philox4x32-10 (Salmon et al., SC'11), word 0 of the output block.
+__device__ __forceinline__ uint32_t philox4x32_10_w0(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                     uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c0;
+}
+
+// Uniform in [0,1) of step t: counter (t, lo32(cycle), hi32(cycle), 0), key = seed.
+__device__ __forceinline__ float walk_uniform(uint64_t seed, uint64_t cycle, int t) {
+  const uint32_t w = philox4x32_10_w0(static_cast<uint32_t>(t), static_cast<uint32_t>(cycle),
+                                      static_cast<uint32_t>(cycle >> 32), 0u,
+                                      static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  return static_cast<float>(w >> 8) * 0x1p-24f;
+}
+
+// The successor slot chosen from one score row of 16, and (if q) the row's draft
+// distribution.  T == 0: the lowest slot holding the maximum, q one-hot.
+// T > 0: p_j = exp((S_j - max)/T), Z = sum in slot order, the first j with
+// u Z < p_0 + ... + p_j (else the last j with p_j > 0), q = p / Z.  `row` may
+// alias `q` (the row is read completely first).
+__device__ __forceinline__ int walk_row_choice(const float* row, float T, float u, float* q) {
+  float v[kCand];
+#pragma unroll
+  for (int j = 0; j < kCand; ++j) v[j] = row[j];
+  int pick = 0;
+  if (T == 0.f) {
+    float best = v[0];
+#pragma unroll
+    for (int j = 1; j < kCand; ++j)
+      if (v[j] > best) {
+        best = v[j];
+        pick = j;
+      }
+    if (q)
+#pragma unroll
+      for (int j = 0; j < kCand; ++j) q[j] = j == pick ? 1.f : 0.f;
+    return pick;
+  }
+  float m = v[0];
+#pragma unroll
+  for (int j = 1; j < kCand; ++j) m = fmaxf(m, v[j]);
+  float Z = 0.f;
+#pragma unroll
+  for (int j = 0; j < kCand; ++j) {
+    v[j] = expf((v[j] - m) / T);
+    Z += v[j];
+  }
+  const float uZ = u * Z;
+  float cum = 0.f;
+  pick = -1;
+#pragma unroll
+  for (int j = 0; j < kCand; ++j) {
+    cum += v[j];
+    if (pick < 0 && uZ < cum) pick = j;
+  }
+  if (pick < 0) {
+    pick = 0;
+#pragma unroll
+    for (int j = 0; j < kCand; ++j)
+      if (v[j] > 0.f) pick = j;
+  }
+  if (q)
+#pragma unroll
+    for (int j = 0; j < kCand; ++j) q[j] = v[j] / Z;
+  return pick;
 }
 
 }  // namespace dfl2

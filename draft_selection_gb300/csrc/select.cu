@@ -3,138 +3,307 @@
 //   S_t(a,b) = U_t(b) + <A(a) ⊙ H(h_t), B(b)>,
 //   A(a) = W_A E[a], B(b) = W_B E[b], H(h) = sigmoid(W_H h)  (W_* [256,d]).
 //
-// Two stages:
-//   1. projections: every candidate row (the verified token, then 16 per
-//      position) is gathered from E and multiplied by [W_A; W_B]^T into
-//      P [M,512] fp32; the hidden states are multiplied by W_H^T and passed
-//      through the sigmoid into H [B*L,256].
-//   2. pair kernel: one CTA per (sequence, position) forms the 16x16 scores
-//      from the previous position's A rows, the gate and this position's B rows.
+// Stage 1, one tcgen05 launch with three GEMM problems (C = rows x W^T, K = d):
+//   PA: the rows whose A(.) is needed (the verified token, then the 16
+//       candidates of positions 0..L-2), gathered from E, times W_A^T;
+//   PB: the candidates of positions 0..L-1, gathered from E, times W_B^T;
+//   GH: the hidden states times W_H^T (pre-sigmoid).
+// Tiles are 128 rows x 256 columns, K in blocks of 64.  W tiles arrive by TMA
+// (128-byte swizzle); the gathered rows by 16-byte cp.async written in the same
+// swizzle; the accumulator lives in TMEM (256 columns).  When there are too few
+// tiles to fill the GPU (batch 1), K is split over the CTAs of a thread-block
+// cluster: each CTA parks its fp32 partial tile in its own shared memory and
+// every CTA sums one slice of rows across the cluster through distributed
+// shared memory, in rank order, so the result is deterministic and no partial
+// ever reaches HBM.
+//
+// Stage 2, the pair kernel: one CTA per (sequence, position) forms the 16x16
+// scores from the previous position's A rows, the gate and this position's B
+// rows.  In the fused tail it also takes the walk's decision for each of its
+// 16 rows, and the last CTA of each sequence follows the chosen slots.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+
 #include "dfl2_internal.cuh"
 
 namespace dfl2 {
 namespace {
 
-constexpr int kProjBM = 64, kProjBN = 64, kProjBK = 32;
+constexpr int kBM = 128, kBN = 256, kBK = 64, kGStages = 4;
+constexpr int kAStage = kBM * kBK * 2;  // 16 KB
+constexpr int kBStage = kBN * kBK * 2;  // 32 KB
+constexpr int kGemmThreads = 256;       // warps 0-3 load, warp 4 issues MMAs, warps 4-7 drain TMEM
+constexpr int kGemmTargetCtas = 148;
+constexpr int kMaxClusterSplits = 8;       // portable cluster size
+constexpr int kRedPitch = kBN + 4;         // fp32 row pitch of the on-chip partial tile
+constexpr size_t kGemmSmem = 1024 + size_t(kGStages) * (kAStage + kBStage) + 256;
+static_assert(size_t(kBM) * kRedPitch * 4 <= size_t(kGStages) * (kAStage + kBStage),
+              "the partial tile reuses the operand stages");
+constexpr uint32_t kTmemCols = 256;
 
-struct ProjArgs {
-  // A operand rows: gathered from `table` by token id (gather = 1), or the
-  // consecutive rows of `table` (gather = 0).
-  const __nv_bfloat16* table;
-  int gather;
-  const int32_t* cand_idx;  // [B,L,16]
-  const int32_t* verified;  // [B]
-  int L, V;
-  int M, N, d;
-  uint32_t* err;
-  const __nv_bfloat16* W0;  // output columns 0..255
-  const __nv_bfloat16* W1;  // output columns 256..511 (N == 512)
-  float* out;               // [M, N]
-  int sigmoid;
+enum RowKind : int { kRowsPA = 0, kRowsPB = 1, kRowsHidden = 2 };
+
+struct GemmProblem {
+  int kind;     // RowKind
+  int M;        // rows
+  int mtiles;   // ceil(M / 128)
+  float* out;   // [M][256]
 };
 
-__device__ __forceinline__ const __nv_bfloat16* proj_row(const ProjArgs& a, int m) {
-  if (!a.gather) return a.table + size_t(m) * a.d;
-  const int per_seq = kCand * a.L + 1;
-  const int b = m / per_seq, q = m % per_seq;
-  const int32_t tok = q == 0 ? a.verified[b] : a.cand_idx[size_t(b) * a.L * kCand + (q - 1)];
+struct GemmArgs {
+  GemmProblem prob[3];
+  int tiles_before[3];  // tiles of the problems before this one
+  int splits, kps, kblocks;  // splits = cluster size along K
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* hidden;
+  const int32_t* cand_idx;  // [B,L,16]
+  const int32_t* verified;  // [B]
+  int L, V, d;
+  uint32_t* err;
+};
+
+// Source row of A for row m of a problem, or nullptr (zero row).
+__device__ __forceinline__ const __nv_bfloat16* a_row(const GemmArgs& a, int kind, int m, int M) {
+  if (m >= M) return nullptr;
+  if (kind == kRowsHidden) return a.hidden + size_t(m) * a.d;
+  int32_t tok;
+  if (kind == kRowsPA) {
+    const int per = kCand * (a.L - 1) + 1;
+    const int b = m / per, q = m % per;
+    tok = q == 0 ? a.verified[b] : a.cand_idx[size_t(b) * a.L * kCand + (q - 1)];
+  } else {
+    const int per = kCand * a.L;
+    const int b = m / per, q = m % per;
+    tok = a.cand_idx[size_t(b) * a.L * kCand + q];
+  }
   if (tok < 0 || tok >= a.V) {  // never read outside E: record it and use a zero row
     record_error(a.err, kDevErrBadIndex);
     return nullptr;
   }
-  return a.table + size_t(tok) * a.d;
+  return a.E + size_t(tok) * a.d;
 }
 
-// Plain smem-tiled fp32-FMA GEMM: out[m,n] = sum_c row_m[c] * W(n)[c].
-__global__ void __launch_bounds__(256) proj_fma_kernel(ProjArgs a) {
-  __shared__ float As[kProjBK][kProjBM + 4];
-  __shared__ float Bs[kProjBK][kProjBN + 4];
-  pdl_wait();
-  const int tid = threadIdx.x;
-  const int m0 = blockIdx.x * kProjBM, n0 = blockIdx.y * kProjBN;
-  const int ty = tid / 16, tx = tid % 16;
-  const int lr = tid / 4, lc = (tid % 4) * 8;  // loader: row, 8-wide column chunk
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    proj_tc_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmH) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                   // kGStages x 16 KB
+  uint8_t* sB = smem + size_t(kGStages) * kAStage;      // kGStages x 32 KB
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + size_t(kGStages) * kBStage);
+  uint64_t* empty_bar = full_bar + kGStages;
+  uint64_t* accum_bar = empty_bar + kGStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
 
-  const int am = m0 + lr;
-  const __nv_bfloat16* arow = am < a.M ? proj_row(a, am) : nullptr;
-  const int bn = n0 + lr;
-  const __nv_bfloat16* brow = nullptr;
-  if (bn < a.N) brow = bn < kRank ? a.W0 + size_t(bn) * a.d : a.W1 + size_t(bn - kRank) * a.d;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // CTA -> (m tile, split); the splits of one tile form one cluster
+  const int split = blockIdx.x % a.splits;
+  const int rem = blockIdx.x / a.splits;
+  const int p = rem >= a.tiles_before[2] ? 2 : (rem >= a.tiles_before[1] ? 1 : 0);
+  const GemmProblem& P = a.prob[p];
+  const int m0 = (rem - a.tiles_before[p]) * kBM;
+  const int kb0 = split * a.kps;
+  const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;
+  const CUtensorMap* tmap = p == 0 ? &tmA : (p == 1 ? &tmB : &tmH);
 
-  float acc[4][4] = {};
-  for (int k0 = 0; k0 < a.d; k0 += kProjBK) {
-    uint4 av = arow ? *reinterpret_cast<const uint4*>(arow + k0 + lc) : make_uint4(0, 0, 0, 0);
-    uint4 bv = brow ? *reinterpret_cast<const uint4*>(brow + k0 + lc) : make_uint4(0, 0, 0, 0);
-    const uint32_t ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      As[lc + 2 * e][lr] = __uint_as_float(ar[e] << 16);
-      As[lc + 2 * e + 1][lr] = __uint_as_float(ar[e] & 0xFFFF0000u);
-      Bs[lc + 2 * e][lr] = __uint_as_float(br[e] << 16);
-      Bs[lc + 2 * e + 1][lr] = __uint_as_float(br[e] & 0xFFFF0000u);
+  if (tid == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&full_bar[s], 4 * 32 + 1);  // 128 cp.async arrivals + the TMA expect_tx
+      mbar_init(&empty_bar[s], 1);          // one tcgen05.commit
     }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kProjBK; ++kk) {
-      float av4[4], bv4[4];
+    mbar_init(accum_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(tmap);
+  }
+  if (warp == 4) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // candidates may come from the previous kernel
+
+  if (warp < 4) {
+    // ---- producers: TMA for the W tile, cp.async for the 128 gathered rows ----
+    const int j = tid & 7;  // 16-byte chunk within the 128-byte row
+    const __nv_bfloat16* src[8];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) av4[i] = As[kk][ty * 4 + i];
+    for (int i = 0; i < 8; ++i) src[i] = a_row(a, P.kind, m0 + (tid >> 3) + 16 * i, P.M);
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kGStages;
+      if (it >= kGStages && !mbar_wait(&empty_bar[s], ((it / kGStages) - 1) & 1))
+        record_error(a.err, kDevErrGemm);
+      const int kelem = (kb0 + it) * kBK;
+      if (tid == 0) {
+        mbar_arrive_expect_tx(&full_bar[s], kBStage);
+        tma_load_2d(sB + size_t(s) * kBStage, tmap, kelem, 0, &full_bar[s]);
+      }
+      uint8_t* dstA = sA + size_t(s) * kAStage;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) bv4[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av4[i], bv4[j], acc[i][j]);
+      for (int i = 0; i < 8; ++i) {
+        const int r = (tid >> 3) + 16 * i;
+        void* dst = dstA + r * 128 + ((j ^ (r & 7)) << 4);
+        const __nv_bfloat16* g = src[i] ? src[i] + kelem + j * 8 : a.E;
+        cp_async16(dst, g, src[i] != nullptr);
+      }
+      cp_async_commit();
+      if (it >= 2) {
+        cp_async_wait<2>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full_bar[(it - 2) % kGStages]);
+      }
     }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int it = max(0, nkb - 2); it < nkb; ++it) mbar_arrive(&full_bar[it % kGStages]);
+  } else {
+    if (warp == 4 && lane == 0) {
+      // ---- MMA issuer ----
+      constexpr uint32_t idesc = umma_idesc_bf16(kBM, kBN);
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % kGStages;
+        if (!mbar_wait(&full_bar[s], (it / kGStages) & 1)) record_error(a.err, kDevErrGemm);
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kAStage);
+        const uint64_t bd = umma_desc_sw128(sB + size_t(s) * kBStage);
+#pragma unroll
+        for (int k = 0; k < kBK / 16; ++k)
+          umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(accum_bar);
+    }
+    __syncwarp();
+    // ---- epilogue: TMEM -> registers -> global (one split) or own smem (cluster) ----
+    const int quarter = warp & 3;
+    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrGemm);
+    tc_fence_after();
+    const int lrow = quarter * 32 + lane;
+    const int row = m0 + lrow;
+    float* red = reinterpret_cast<float*>(smem) + size_t(lrow) * kRedPitch;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
+      float4* o = a.splits == 1 ? (row < P.M ? reinterpret_cast<float4*>(P.out + size_t(row) * kBN + c * 32)
+                                             : nullptr)
+                                : reinterpret_cast<float4*>(red + c * 32);
+      if (o) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  if (a.splits == 1) {
     __syncthreads();
+    pdl_launch_dependents();
+    if (warp == 4) {
+      tc_fence_after();
+      tmem_dealloc(tmem, kTmemCols);
+    }
+    return;
+  }
+  // ---- split K: reduce the cluster's partial tiles through distributed smem ----
+  cluster_sync_all();  // every CTA's partial tile is complete (also a CTA barrier)
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  const int S = a.splits;
+  const int rows_per = kBM / S;
+  const int r0 = split * rows_per;
+  const int n4 = rows_per * (kBN / 4);
+  const float* red_base = reinterpret_cast<const float*>(smem);
+  for (int e = tid; e < n4; e += kGemmThreads) {
+    const int lr = r0 + e / (kBN / 4), c4 = e % (kBN / 4);
+    const float* src = red_base + size_t(lr) * kRedPitch + c4 * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < S; ++k) {  // rank order: deterministic
+      const float4 v = dsmem_ld4(dsmem_addr(src, k));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    const int grow = m0 + lr;
+    if (grow < P.M) reinterpret_cast<float4*>(P.out + size_t(grow) * kBN)[c4] = acc;
   }
   pdl_launch_dependents();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
-    if (m >= a.M) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
-      if (n >= a.N) continue;
-      float v = acc[i][j];
-      if (a.sigmoid) v = 1.0f / (1.0f + expf(-v));
-      a.out[size_t(m) * a.N + n] = v;
-    }
-  }
+  cluster_sync_all();  // no CTA leaves while others still read its shared memory
 }
 
 struct PairArgs {
-  const float* P;         // [B*(16L+1), 512]
-  const float* H;         // [B*L, 256]
+  const float* PA;  // [MA][256]
+  const float* PB;  // [MB][256]
+  const float* GH;  // [B*L][256], pre-sigmoid
   const float* cand_val;  // [B,L,16]
   float* scores;          // [B,L,16,16]
   int L;
+  // fused walk (walk == 0: scores only)
+  int walk;
+  float T;
+  const uint64_t* seeds;
+  uint64_t cycle;
+  const int32_t* cand_idx;  // [B,L,16]
+  int32_t* tokens;          // [B,L]
+  int32_t* slots;           // [B,L] or null
+  float* q;                 // [B,L,16] or null
+  uint32_t* tickets;        // [B], zero between calls
+  int32_t* choice;          // [B*L][16] workspace
+  float* qrows;             // [B*L][16][16] workspace
 };
 
 // One CTA per (sequence b, position t); thread (i, j) forms S_t(a_i, b_j).
 __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
-  __shared__ float Gs[kCand][kRank + 1];  // A(a_i) ⊙ H(h_t)
-  __shared__ float Bsh[kCand][kRank + 1]; // B(b_j)
+  __shared__ float Gs[kCand][kRank + 1];   // A(a_i) ⊙ H(h_t)
+  __shared__ float Bsh[kCand][kRank + 1];  // B(b_j)
+  __shared__ float Hs[kRank];
   __shared__ float U[kCand];
+  __shared__ float Srow[kCand][kCand + 1];
+  __shared__ int path[128];
+  __shared__ uint32_t last;
   pdl_wait();
   const int cell = blockIdx.x;
   const int b = cell / a.L, t = cell % a.L;
-  const int per_seq = kCand * a.L + 1;
-  const size_t seq0 = size_t(b) * per_seq;
   const int npred = t == 0 ? 1 : kCand;
-  const float* Hrow = a.H + size_t(cell) * kRank;
-  for (int e = threadIdx.x; e < kCand * kRank; e += blockDim.x) {
-    const int i = e / kRank, q = e % kRank;
-    if (i < npred) {
-      const size_t prow = t == 0 ? seq0 : seq0 + 1 + size_t(kCand) * (t - 1) + i;
-      Gs[i][q] = a.P[prow * (2 * kRank) + q] * Hrow[q];
-    }
-    Bsh[i][q] = a.P[(seq0 + 1 + size_t(kCand) * t + i) * (2 * kRank) + kRank + q];
+  const size_t rowA0 =
+      size_t(b) * (kCand * (a.L - 1) + 1) + (t == 0 ? 0 : 1 + size_t(kCand) * (t - 1));
+  const size_t rowB0 = size_t(b) * kCand * a.L + size_t(kCand) * t;
+  const int tid = threadIdx.x;
+  {
+    const float g = a.GH[size_t(cell) * kRank + tid];
+    Hs[tid] = 1.0f / (1.0f + expf(-g));
   }
-  if (threadIdx.x < kCand) U[threadIdx.x] = a.cand_val[size_t(cell) * kCand + threadIdx.x];
+  // A and B rows: 16 rows x 64 float4 each; all loads issued before any use.
+  float4 va[4], vb[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = tid + 256 * k;
+    const int i = e >> 6, q4 = e & 63;
+    va[k] = i < npred ? reinterpret_cast<const float4*>(a.PA + (rowA0 + i) * kRank)[q4]
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    vb[k] = reinterpret_cast<const float4*>(a.PB + (rowB0 + i) * kRank)[q4];
+  }
+  if (tid < kCand) U[tid] = a.cand_val[size_t(cell) * kCand + tid];
+  __syncthreads();  // Hs complete
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e = tid + 256 * k;
+    const int i = e >> 6, c = 4 * (e & 63);
+    Gs[i][c + 0] = va[k].x * Hs[c + 0];
+    Gs[i][c + 1] = va[k].y * Hs[c + 1];
+    Gs[i][c + 2] = va[k].z * Hs[c + 2];
+    Gs[i][c + 3] = va[k].w * Hs[c + 3];
+    Bsh[i][c + 0] = vb[k].x;
+    Bsh[i][c + 1] = vb[k].y;
+    Bsh[i][c + 2] = vb[k].z;
+    Bsh[i][c + 3] = vb[k].w;
+  }
   __syncthreads();
-  const int i = threadIdx.x / kCand, j = threadIdx.x % kCand;
+  const int i = tid / kCand, j = tid % kCand;
   float s;
   if (i < npred) {
     s = 0.f;
@@ -144,9 +313,66 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
   } else {
     s = -INFINITY;
   }
+  a.scores[size_t(cell) * kCand * kCand + tid] = s;
+  if (!a.walk) {
+    pdl_launch_dependents();
+    return;
+  }
+
+  // ---- fused walk: the decision of every row of this position ----
+  Srow[i][j] = s;
+  __syncthreads();
+  if (tid < npred) {
+    const float u = a.T > 0.f ? walk_uniform(a.seeds[b], a.cycle, t) : 0.f;
+    float qv[kCand];
+    const int c = walk_row_choice(&Srow[tid][0], a.T, u, qv);
+    a.choice[size_t(cell) * kCand + tid] = c;
+    float4* qo = reinterpret_cast<float4*>(a.qrows + (size_t(cell) * kCand + tid) * kCand);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) qo[k] = make_float4(qv[4 * k], qv[4 * k + 1], qv[4 * k + 2], qv[4 * k + 3]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const uint32_t ticket = atomicInc(&a.tickets[b], static_cast<unsigned>(a.L - 1));
+    last = ticket == static_cast<uint32_t>(a.L - 1);
+  }
+  __syncthreads();
+  if (!last) {
+    pdl_launch_dependents();
+    return;
+  }
+  // ---- last CTA of sequence b: follow the chosen slots from the verified token ----
+  __threadfence();
+  const int* ch = a.choice + size_t(b) * a.L * kCand;
+  int* chs = reinterpret_cast<int*>(&Gs[0][0]);  // L x 16 choices (L <= 128 fits)
+  for (int e = tid; e < a.L * kCand; e += 256) chs[e] = __ldcg(ch + e);
+  __syncthreads();
+  if (tid == 0) {
+    int prev = 0;
+    for (int tt = 0; tt < a.L; ++tt) {
+      prev = chs[tt * kCand + prev] & (kCand - 1);
+      path[tt] = prev;
+    }
+  }
+  __syncthreads();
+  for (int tt = tid; tt < a.L; tt += 256) {
+    const size_t c2 = size_t(b) * a.L + tt;
+    a.tokens[c2] = a.cand_idx[c2 * kCand + path[tt]];
+    if (a.slots) a.slots[c2] = path[tt];
+  }
+  if (a.q) {
+    for (int e = tid; e < a.L * kCand; e += 256) {
+      const int tt = e / kCand, k = e % kCand;
+      const size_t c2 = size_t(b) * a.L + tt;
+      const int row = tt == 0 ? 0 : path[tt - 1];  // step tt draws from its predecessor's row
+      a.q[c2 * kCand + k] = __ldcg(a.qrows + (c2 * kCand + row) * kCand + k);
+    }
+  }
   pdl_launch_dependents();
-  a.scores[size_t(cell) * kCand * kCand + threadIdx.x] = s;
 }
+
+bool g_gemm_attr[64];
 
 }  // namespace
 
@@ -155,10 +381,27 @@ SelectPlan select_plan(int B, int L, int d) {
   p.B = B;
   p.L = L;
   p.d = d;
-  p.M = B * (kCand * L + 1);
-  p.P_off = 256;
-  p.H_off = align_up(p.P_off + size_t(p.M) * 2 * kRank * sizeof(float), 256);
-  p.ws_bytes = align_up(p.H_off + size_t(B) * L * kRank * sizeof(float), 256);
+  p.MA = B * (kCand * (L - 1) + 1);
+  p.MB = B * kCand * L;
+  p.MH = B * L;
+  p.kblocks = d / kBK;
+  const int tiles = (p.MA + kBM - 1) / kBM + (p.MB + kBM - 1) / kBM + (p.MH + kBM - 1) / kBM;
+  // Split K (over a cluster) only when the tiles cannot fill the GPU: the
+  // largest power of two <= 8 that keeps tiles*splits within one wave.
+  int splits = 1;
+  while (splits * 2 <= kMaxClusterSplits && tiles * splits * 2 <= kGemmTargetCtas &&
+         splits * 2 <= p.kblocks)
+    splits *= 2;
+  p.splits = splits;
+  p.kps = (p.kblocks + splits - 1) / splits;
+  p.PA_off = 256;
+  p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
+  p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);
+  p.ticket_off = align_up(p.GH_off + size_t(p.MH) * kRank * 4, 256);
+  p.choice_off = align_up(p.ticket_off + size_t(B) * 4, 256);
+  p.q_off = align_up(p.choice_off + size_t(B) * L * kCand * 4, 256);
+  p.ws_bytes = align_up(p.q_off + size_t(B) * L * kCand * kCand * 4, 256);
+  p.M = p.MA;
   return p;
 }
 
@@ -166,41 +409,126 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
                           const int32_t* verified, const __nv_bfloat16* hidden,
                           const __nv_bfloat16* E, const __nv_bfloat16* W_A,
                           const __nv_bfloat16* W_B, const __nv_bfloat16* W_H, int V,
-                          float* scores, void* ws, cudaStream_t s, bool pdl) {
-  float* P = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + p.P_off);
-  float* H = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + p.H_off);
-  ProjArgs pa{};
-  pa.table = E;
-  pa.gather = 1;
-  pa.cand_idx = cand_idx;
-  pa.verified = verified;
-  pa.L = p.L;
-  pa.V = V;
-  pa.err = device_error_word();
-  pa.M = p.M;
-  pa.N = 2 * kRank;
-  pa.d = p.d;
-  pa.W0 = W_A;
-  pa.W1 = W_B;
-  pa.out = P;
-  pa.sigmoid = 0;
-  cudaError_t e = launch_k(proj_fma_kernel, dim3((pa.M + kProjBM - 1) / kProjBM, pa.N / kProjBN),
-                           dim3(256), 0, s, pdl, pa);
+                          float* scores, const WalkFuse* walk, void* ws, cudaStream_t s,
+                          bool pdl) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  ProjArgs ha = pa;
-  ha.table = hidden;
-  ha.gather = 0;
-  ha.M = p.B * p.L;
-  ha.N = kRank;
-  ha.W0 = W_H;
-  ha.W1 = nullptr;
-  ha.out = H;
-  ha.sigmoid = 1;
-  e = launch_k(proj_fma_kernel, dim3((ha.M + kProjBM - 1) / kProjBM, ha.N / kProjBN), dim3(256),
-               0, s, pdl, ha);
+  if (!g_gemm_attr[dev & 63]) {
+    e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmem));
+    if (e != cudaSuccess) return e;
+    g_gemm_attr[dev & 63] = true;
+  }
+  alignas(64) CUtensorMap tA, tB, tH;
+  if (!tensor_map_bf16(W_A, kRank, p.d, kBN, &tA) || !tensor_map_bf16(W_B, kRank, p.d, kBN, &tB) ||
+      !tensor_map_bf16(W_H, kRank, p.d, kBN, &tH))
+    return cudaErrorInvalidValue;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* PA = reinterpret_cast<float*>(w + p.PA_off);
+  float* PB = reinterpret_cast<float*>(w + p.PB_off);
+  float* GH = reinterpret_cast<float*>(w + p.GH_off);
+  GemmArgs g{};
+  const int Ms[3] = {p.MA, p.MB, p.MH};
+  float* outs[3] = {PA, PB, GH};
+  int before = 0;
+  for (int i = 0; i < 3; ++i) {
+    g.prob[i].kind = i;
+    g.prob[i].M = Ms[i];
+    g.prob[i].mtiles = (Ms[i] + kBM - 1) / kBM;
+    g.prob[i].out = outs[i];
+    g.tiles_before[i] = before;
+    before += g.prob[i].mtiles;
+  }
+  g.splits = p.splits;
+  g.kps = p.kps;
+  g.kblocks = p.kblocks;
+  g.E = E;
+  g.hidden = hidden;
+  g.cand_idx = cand_idx;
+  g.verified = verified;
+  g.L = p.L;
+  g.V = V;
+  g.d = p.d;
+  g.err = device_error_word();
+  e = launch_kc(proj_tc_kernel, dim3(before * p.splits), dim3(kGemmThreads), kGemmSmem, s, pdl,
+                p.splits, g, tA, tB, tH);
   if (e != cudaSuccess) return e;
-  PairArgs qa{P, H, cand_val, scores, p.L};
+  PairArgs qa{};
+  qa.PA = PA;
+  qa.PB = PB;
+  qa.GH = GH;
+  qa.cand_val = cand_val;
+  qa.scores = scores;
+  qa.L = p.L;
+  if (walk) {
+    qa.walk = 1;
+    qa.T = walk->T;
+    qa.seeds = walk->seeds;
+    qa.cycle = walk->cycle;
+    qa.cand_idx = cand_idx;
+    qa.tokens = walk->tokens;
+    qa.slots = walk->slots;
+    qa.q = walk->q;
+    qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
+    qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
+    qa.qrows = reinterpret_cast<float*>(w + p.q_off);
+  }
   return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(256), 0, s, pdl, qa);
+}
+
+// ---- tensor maps ------------------------------------------------------------------
+namespace {
+struct TmapEntry {
+  int dev;
+  const void* base;
+  uint64_t rows, cols;
+  uint32_t box_rows;
+  CUtensorMap map;
+};
+std::mutex g_tmap_mu;
+TmapEntry g_tmap_cache[32];
+int g_tmap_n = 0, g_tmap_next = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+}  // namespace
+
+bool tensor_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     void* out128) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  std::lock_guard<std::mutex> lock(g_tmap_mu);
+  for (int i = 0; i < g_tmap_n; ++i) {
+    const TmapEntry& t = g_tmap_cache[i];
+    if (t.dev == dev && t.base == base && t.rows == rows && t.cols == cols &&
+        t.box_rows == box_rows) {
+      memcpy(out128, &t.map, sizeof(CUtensorMap));
+      return true;
+    }
+  }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  CUtensorMap m;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  TmapEntry& t = g_tmap_cache[g_tmap_next];
+  t = TmapEntry{dev, base, rows, cols, box_rows, m};
+  g_tmap_next = (g_tmap_next + 1) % 32;
+  g_tmap_n = std::min(g_tmap_n + 1, 32);
+  memcpy(out128, &m, sizeof(CUtensorMap));
+  return true;
 }
 
 }  // namespace dfl2

@@ -32,8 +32,10 @@ constexpr int kTileBytes = 8192;
 constexpr int kStages = 8;
 constexpr int kMaxGrid = 2048;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr size_t kSmemBytes =
-    size_t(kStages) * kTileBytes + 2 * kStages * sizeof(uint64_t) + 2 * kConsumerWarps * kCand * sizeof(uint64_t);
+constexpr size_t kSmemBytes = size_t(kStages) * kTileBytes + 2 * kStages * sizeof(uint64_t) +
+                              2 * kConsumerWarps * kCand * sizeof(uint64_t) +
+                              (2 + kConsumerWarps) * sizeof(uint32_t);
+constexpr int kMergeBatch = 4;  // partial lists each warp loads at once in the final merge
 
 struct TopkArgs {
   const uint8_t* logits;
@@ -84,6 +86,20 @@ __device__ __forceinline__ uint64_t warp_merge32_desc(uint64_t x, int lane) {
   return x;
 }
 
+__device__ __forceinline__ uint64_t shfl_up64(uint64_t v, int d) {
+  uint32_t lo = __shfl_up_sync(kFull, static_cast<uint32_t>(v), d);
+  uint32_t hi = __shfl_up_sync(kFull, static_cast<uint32_t>(v >> 32), d);
+  return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Insert one key (the same in every lane) into the descending list in lanes 0..15.
+__device__ __forceinline__ uint64_t insert_one(uint64_t list, uint64_t key, int lane) {
+  const int pos = __popc(__ballot_sync(kFull, lane < 16 && list > key));
+  const uint64_t up = shfl_up64(list, 1);
+  if (lane >= 16) return 0ull;
+  return lane < pos ? list : (lane == pos ? key : up);
+}
+
 // Merge 16 descending keys held in lanes 0..15 of `cand` into `list`.
 __device__ __forceinline__ uint64_t merge_sorted16(uint64_t list, uint64_t cand, int lane) {
   const uint64_t rev = shfl64(cand, 31 - lane);
@@ -117,21 +133,50 @@ struct WarpTop {
   float thr_v;    // its value
 };
 
+// cta_thr: the best 16th value any warp of this CTA holds for the current row
+// (as an order-preserving uint32, 0 = none yet).  Some warp holds 16 elements
+// at or above it, so an element strictly below it cannot be in the row's top 16.
 template <int EPV>
 __device__ __forceinline__ void process_block(WarpTop& w, const float (&f)[EPV], bool valid,
-                                              uint32_t idx0, int lane) {
+                                              uint32_t idx0, int lane, uint32_t* cta_thr,
+                                              uint32_t* warp_v2, int warp) {
   float m = f[0];
 #pragma unroll
   for (int e = 1; e < EPV; ++e) m = fmaxf(m, f[e]);
-  const bool hit = valid && (w.thr == 0 || m > w.thr_v);
+  const uint32_t shared_o = *reinterpret_cast<volatile uint32_t*>(cta_thr);
+  const float shared_v = shared_o == 0u ? -INFINITY : unord_f32(shared_o);
+  const bool hit = valid && !(m < shared_v) && (w.thr == 0 || m > w.thr_v);
   if (!__any_sync(kFull, hit)) return;
   uint32_t pend = 0;
-  if (valid) {
+  if (w.thr == 0) {
+    // Empty list: seed it with the 16 best lane maxima in one sort.
+    uint64_t lm = 0;
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint64_t k = make_key(f[e], idx0 + e);
+        lm = k > lm ? k : lm;
+      }
+    }
+    const uint64_t srt = warp_sort32_desc(lm, lane);
+    w.list = merge_sorted16(w.list, srt, lane);
+    w.thr = shfl64(w.list, 15);
+    w.thr_v = unord_f32(static_cast<uint32_t>(w.thr >> 32));
+    if (valid) {
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const uint64_t k = make_key(f[e], idx0 + e);
+        if (k > w.thr && k != lm && !(f[e] < shared_v)) pend |= 1u << e;
+      }
+    }
+  } else if (valid) {
 #pragma unroll
     for (int e = 0; e < EPV; ++e)
-      if (make_key(f[e], idx0 + e) > w.thr) pend |= 1u << e;
+      if (make_key(f[e], idx0 + e) > w.thr && !(f[e] < shared_v)) pend |= 1u << e;
   }
-  while (__any_sync(kFull, pend != 0)) {
+  while (true) {
+    const unsigned who = __ballot_sync(kFull, pend != 0);
+    if (!who) break;
     uint64_t cand = 0;
     if (pend) {
       const int e = __ffs(pend) - 1;
@@ -141,8 +186,19 @@ __device__ __forceinline__ void process_block(WarpTop& w, const float (&f)[EPV],
       for (int e2 = 1; e2 < EPV; ++e2) v = (e2 == e) ? f[e2] : v;
       cand = make_key(v, idx0 + e);
     }
-    cand = warp_sort32_desc(cand, lane);
-    w.list = merge_sorted16(w.list, cand, lane);
+    if (__popc(who) <= 2) {
+      // Few candidates (the common case once the list is warm): insert each directly.
+      unsigned rest = who;
+      while (rest) {
+        const int src = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const uint64_t k = shfl64(cand, src);
+        if (k > shfl64(w.list, 15)) w.list = insert_one(w.list, k, lane);
+      }
+    } else {
+      cand = warp_sort32_desc(cand, lane);
+      w.list = merge_sorted16(w.list, cand, lane);
+    }
     w.thr = shfl64(w.list, 15);
     w.thr_v = unord_f32(static_cast<uint32_t>(w.thr >> 32));
     if (pend) {
@@ -150,6 +206,18 @@ __device__ __forceinline__ void process_block(WarpTop& w, const float (&f)[EPV],
       for (int e = 0; e < EPV; ++e)
         if (((pend >> e) & 1u) && !(make_key(f[e], idx0 + e) > w.thr)) pend &= ~(1u << e);
     }
+  }
+  // Publish a tighter CTA bound: besides this warp's 16th value, the smallest of
+  // the eight warps' 2nd-best values (8 warps x 2 elements at or above it).
+  const uint64_t second = shfl64(w.list, 1);
+  if (lane == 0) {
+    if (second != 0) warp_v2[warp] = static_cast<uint32_t>(second >> 32);
+    uint32_t m2 = 0xFFFFFFFFu;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) m2 = min(m2, *reinterpret_cast<volatile uint32_t*>(&warp_v2[k]));
+    const uint32_t own = w.thr != 0 ? static_cast<uint32_t>(w.thr >> 32) : 0u;
+    const uint32_t bound = max(own, m2);
+    if (bound != 0u) atomicMax(cta_thr, bound);
   }
 }
 
@@ -167,6 +235,9 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kTileBytes);
   uint64_t* empty_bar = full_bar + kStages;
   uint64_t* merge_buf = empty_bar + kStages;  // [2][kConsumerWarps][16]
+  uint32_t* cta_thr = reinterpret_cast<uint32_t*>(merge_buf + 2 * kConsumerWarps * kCand);
+  uint32_t* last_flag = cta_thr + 1;
+  uint32_t* warp_v2 = cta_thr + 2;  // [kConsumerWarps] each warp's 2nd-best value, ordered
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long T = a.total_tiles;
@@ -181,6 +252,8 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
     fence_mbar_init();
+    *cta_thr = 0u;
+    for (int k = 0; k < kConsumerWarps; ++k) warp_v2[k] = 0u;
   }
   __syncthreads();
   pdl_wait();  // the logits may come from the previous kernel on the stream
@@ -222,7 +295,8 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
         uint4 q = valid ? tile[v] : make_uint4(0u, 0u, 0u, 0u);
         float f[EPV];
         unpack<EPV>(q, f);
-        process_block<EPV>(w, f, valid, elem_base + static_cast<uint32_t>(v) * EPV, lane);
+        process_block<EPV>(w, f, valid, elem_base + static_cast<uint32_t>(v) * EPV, lane,
+                           cta_thr, warp_v2, warp);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
@@ -231,35 +305,59 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
     // Merge the warps' lists for this row segment.
     uint64_t* mb = merge_buf + (seg & 1) * kConsumerWarps * kCand;
     if (lane < kCand) mb[warp * kCand + lane] = w.list;
+    const int c_first = owner_cta(row * tpr, T, G);
+    const int c_last = owner_cta(row * tpr + tpr - 1, T, G);
+    const int ncontrib = c_last - c_first + 1;
+    uint64_t* part = a.partial + size_t(row) * a.max_contrib * kCand;
     named_sync(1, kConsumerWarps * 32);
     if (warp == 0) {
       uint64_t x = w.list;
       for (int w2 = 1; w2 < kConsumerWarps; ++w2)
         x = warp_merge32_desc(lane < 16 ? x : mb[w2 * kCand + ((31 - lane) & 15)], lane);
-      const int c_first = owner_cta(row * tpr, T, G);
-      const int c_last = owner_cta(row * tpr + tpr - 1, T, G);
-      const int ncontrib = c_last - c_first + 1;
+      uint32_t last = 0;
       if (ncontrib == 1) {
         write_row(a, row, x, lane);
       } else {
-        uint64_t* part = a.partial + size_t(row) * a.max_contrib * kCand;
         if (lane < kCand) part[(c - c_first) * kCand + lane] = x;
         __threadfence();
         __syncwarp();
         uint32_t ticket = 0;
         if (lane == 0) ticket = atomicInc(&a.tickets[row], static_cast<unsigned>(ncontrib - 1));
-        ticket = __shfl_sync(kFull, ticket, 0);
-        if (ticket == static_cast<uint32_t>(ncontrib - 1)) {
-          __threadfence();
-          const unsigned long long* pp = reinterpret_cast<const unsigned long long*>(part);
-          uint64_t acc = __ldcg(pp + (lane & 15));
-          for (int k = 1; k < ncontrib; ++k) {
-            const uint64_t y = __ldcg(pp + k * kCand + ((31 - lane) & 15));
-            acc = warp_merge32_desc(lane < 16 ? acc : y, lane);
-          }
-          write_row(a, row, acc, lane);
-        }
+        last = __shfl_sync(kFull, ticket, 0) == static_cast<uint32_t>(ncontrib - 1);
       }
+      if (lane == 0) {
+        *last_flag = last;
+        *cta_thr = 0u;  // the next segment is another row
+        for (int k = 0; k < kConsumerWarps; ++k) warp_v2[k] = 0u;
+      }
+    }
+    named_sync(1, kConsumerWarps * 32);
+    if (*last_flag) {
+      // Last CTA of a split row: every warp merges a share of the partial lists,
+      // loading kMergeBatch lists at a time, then warp 0 merges the warps' results.
+      __threadfence();
+      const unsigned long long* pp = reinterpret_cast<const unsigned long long*>(part);
+      uint64_t acc = 0;
+      for (int k0 = warp; k0 < ncontrib; k0 += kConsumerWarps * kMergeBatch) {
+        uint64_t y[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+          const int k = k0 + u * kConsumerWarps;
+          y[u] = k < ncontrib ? __ldcg(pp + k * kCand + ((31 - lane) & 15)) : 0ull;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) acc = warp_merge32_desc(lane < 16 ? acc : y[u], lane);
+      }
+      uint64_t* mb2 = merge_buf + ((seg + 1) & 1) * kConsumerWarps * kCand;
+      if (lane < kCand) mb2[warp * kCand + lane] = acc;
+      named_sync(1, kConsumerWarps * 32);
+      if (warp == 0) {
+        uint64_t x = acc;
+        for (int w2 = 1; w2 < kConsumerWarps; ++w2)
+          x = warp_merge32_desc(lane < 16 ? x : mb2[w2 * kCand + ((31 - lane) & 15)], lane);
+        write_row(a, row, x, lane);
+      }
+      named_sync(1, kConsumerWarps * 32);
     }
     ++seg;
   }

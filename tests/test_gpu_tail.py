@@ -60,6 +60,10 @@ def check_tail(w, lg, inp, T, seeds, cycle, seqs):
     ref = oracle_select_subset(ci, cv, inp["verified"].cpu(), inp, seqs)
     worst = assert_scores_close(g["scores"][seqs], ref, w.name)
     allowed = replay_walk(ref, g["slots"][seqs], T, seeds[seqs], cycle, what=f"{w.name} T={T}")
+    # q: the draft distribution of each step's row, where the paths agree with the oracle's
+    _, rs, rq = oracle.walk(ref, g["cand_idx"][seqs], T, seeds[seqs], cycle)
+    same = np.all(g["slots"][seqs] == rs, axis=1)
+    np.testing.assert_allclose(g["q"][seqs][same], rq[same], rtol=1e-3, atol=1e-6)
     np.testing.assert_array_equal(
         g["tokens"], np.take_along_axis(g["cand_idx"], g["slots"][..., None].astype(np.int64),
                                         2)[..., 0])
