@@ -340,8 +340,8 @@ dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* b
                        const uint16_t* W_c, int B, int L, int d, uint16_t* y,
                        dfl2_stream stream) {
   DFL2_TRY(check_shape(B, L));
-  if (d < dfl2::kGroup || d % dfl2::kGroup != 0 || d > 32768)
-    return fail(DFL2_ERR_UNSUPPORTED, "d=%d: the conv needs a multiple of 16 up to 32768", d);
+  if (d < dfl2::kGroup || d % dfl2::kGroup != 0 || d > 65536)
+    return fail(DFL2_ERR_UNSUPPORTED, "d=%d: the conv needs a multiple of 16 up to 65536", d);
   const Ptrs ptrs = {{x, "x"}, {x_prev, "x_prev"}, {base, "base"}, {W_c, "W_c"}, {y, "y"}};
   DFL2_TRY(check_host(ptrs));
   const size_t ybytes = size_t(B) * L * d * 2;

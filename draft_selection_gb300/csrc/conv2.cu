@@ -3,140 +3,265 @@
 //   y_t = k_{t,0} ⊙ x_t + k_{t,1} ⊙ x_{t-1},  x_{-1} = the verified token's representation,
 //   k_{t,j,c} = base[j,c] + corr[t,j,c/16],   corr[t,j,g] = sum_c W_c[j*G+g, c] x_t[c].
 //
-// One CTA owns NG correction groups (2*NG rows of W_c: both taps) for a tile
-// of TL positions of one sequence.  It stages x_{t0-1..t0+TL-1} in shared
-// memory, streams its W_c rows once, forms the corrections with fp32 FMAs and
-// writes y for the NG*16 channels it owns: correction and mixing are fused,
-// so the corrections never reach HBM.
+// The corrections are a GEMM, corr = X W_sel^T, with the B*L positions as rows
+// and, per CTA, the 2*NG W_c rows of NG correction groups (tap 0 and tap 1 of
+// the same groups) as columns.  It runs on tcgen05: 128-row tiles, K in blocks
+// of 64, both operands staged by 16-byte cp.async in the 128-byte swizzle
+// (zero fill past the ends, so any d that is a multiple of 16 works), the
+// accumulator in TMEM.  The epilogue applies the 2-tap mix for the CTA's
+// 16*NG channels, reading x_t and x_{t-1} (x_prev at t = 0) and writing y in
+// bf16: the corrections never leave the chip.  With few positions (batch 1),
+// K is split over a thread-block cluster and the partial corrections are summed
+// through distributed shared memory, each CTA then mixing its slice of rows.
+#include <algorithm>
+
 #include "dfl2_internal.cuh"
 
 namespace dfl2 {
 namespace {
 
-constexpr int kConvThreads = 256;
-constexpr int kConvWarps = kConvThreads / 32;
-constexpr int kMaxTL = 16;
-constexpr int kMaxNG = 8;
-constexpr size_t kConvXBudget = 96 * 1024;  // bytes of staged x per CTA
+constexpr int kCBM = 128, kCBK = 64, kCStages = 4, kCThreads = 256;
+constexpr int kCMaxNG = 64;          // groups per CTA: N = 2*NG <= 128
+constexpr int kCMaxSplits = 8;       // portable cluster size
+constexpr int kCAStage = kCBM * kCBK * 2;  // 16 KB
 
 struct ConvArgs {
-  const __nv_bfloat16* x;
-  const __nv_bfloat16* x_prev;
-  const float* base;
-  const __nv_bfloat16* W_c;
-  __nv_bfloat16* y;
-  int L, d, G;
-  int TL, NG;
+  const __nv_bfloat16* x;       // [R, d]
+  const __nv_bfloat16* x_prev;  // [B, d]
+  const float* base;            // [2, d]
+  const __nv_bfloat16* W_c;     // [2G, d]
+  __nv_bfloat16* y;             // [R, d]
+  int R, L, d, G;
+  int NG, ntiles, splits, kps, kblocks;
   uint32_t* err;
 };
 
-__device__ __forceinline__ float dot8(const uint4& w, const uint4& x) {
-  const uint32_t wr[4] = {w.x, w.y, w.z, w.w}, xr[4] = {x.x, x.y, x.z, x.w};
-  float s = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    s = fmaf(__uint_as_float(wr[e] << 16), __uint_as_float(xr[e] << 16), s);
-    s = fmaf(__uint_as_float(wr[e] & 0xFFFF0000u), __uint_as_float(xr[e] & 0xFFFF0000u), s);
-  }
-  return s;
+__host__ __device__ constexpr int conv_bstage_bytes(int NG) { return 2 * NG * kCBK * 2; }
+__host__ __device__ constexpr int conv_pitch(int NG) { return 2 * NG + 4; }  // fp32 per row
+
+__host__ __device__ size_t conv_part_bytes(int NG) { return size_t(kCBM) * conv_pitch(NG) * 4; }
+__host__ __device__ size_t conv_stage_area(int NG) {
+  const size_t stages = size_t(kCStages) * (kCAStage + conv_bstage_bytes(NG));
+  const size_t part = conv_part_bytes(NG);
+  return stages > part ? stages : part;
+}
+size_t conv_smem_bytes(int NG) {
+  // [operand stages | partial tile (reuses them)] [corrections] [base slice] [barriers]
+  return 1024 + conv_stage_area(NG) + conv_part_bytes(NG) + size_t(2) * 16 * NG * 4 + 128;
 }
 
-__global__ void __launch_bounds__(kConvThreads) conv2_fma_kernel(ConvArgs a) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  const int d = a.d, G = a.G, TL = a.TL, NG = a.NG;
-  const int g0 = blockIdx.x * NG, t0 = blockIdx.y * TL, b = blockIdx.z;
-  const int tl = min(TL, a.L - t0);  // positions in this tile
-  const int ng = min(NG, G - g0);    // groups in this CTA
-  const int rows = 2 * NG;           // W_c rows (both taps), some unused when ng < NG
-  // layout: xs [(TL+1) rows][d] bf16 | red [kConvWarps][rows][TL] f32 | corr [rows][TL] f32 | bar
-  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
-  float* red = reinterpret_cast<float*>(smem + size_t(TL + 1) * d * 2);
-  float* corr = red + kConvWarps * rows * TL;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(corr + rows * TL);
+__global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constant__ ConvArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int NG = a.NG, N = 2 * NG, pitch = conv_pitch(NG);
+  const int bst = conv_bstage_bytes(NG);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + size_t(kCStages) * kCAStage;
+  float* part = reinterpret_cast<float*>(smem);  // reuses the stages after the mainloop
+  float* corr = reinterpret_cast<float*>(smem + conv_stage_area(NG));
+  float* bslice = corr + size_t(kCBM) * pitch;   // [2][16*NG]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * NG);
+  uint64_t* empty_bar = full_bar + kCStages;
+  uint64_t* accum_bar = empty_bar + kCStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
 
-  if (threadIdx.x == 0) {
-    mbar_init(bar, 1);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % a.splits;
+  const int tile = blockIdx.x / a.splits;
+  const int m0 = (tile / a.ntiles) * kCBM;
+  const int g0 = (tile % a.ntiles) * NG;
+  const int kb0 = split * a.kps;
+  const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;  // >= 1 by construction on the host
+  const uint32_t ncols = N < 32 ? 32u : static_cast<uint32_t>(N);
+
+  if (tid == 0) {
+    for (int s = 0; s < kCStages; ++s) {
+      mbar_init(&full_bar[s], 4 * 32);  // the 128 producer threads
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(accum_bar, 1);
     fence_mbar_init();
   }
+  if (warp == 4) tmem_alloc(tmem_slot, ncols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
   pdl_wait();
-  // Stage x_{t0-1} (x_prev at t0 == 0) and x_{t0..t0+tl-1} with bulk copies:
-  // the rows are contiguous in x, apart from x_prev.
-  const int vec_per_row = d / 8;
-  if (threadIdx.x == 0) {
-    const uint32_t row_bytes = static_cast<uint32_t>(d) * 2;
-    mbar_arrive_expect_tx(bar, row_bytes * (tl + 1));
-    if (t0 == 0) {
-      bulk_g2s(xs, a.x_prev + size_t(b) * d, row_bytes, bar);
-      bulk_g2s(xs + d, a.x + size_t(b) * a.L * d, row_bytes * tl, bar);
-    } else {
-      bulk_g2s(xs, a.x + (size_t(b) * a.L + t0 - 1) * d, row_bytes * (tl + 1), bar);
+  // base slice for the CTA's channels (zero past d)
+  for (int e = tid; e < 2 * 16 * NG; e += kCThreads) {
+    const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
+    bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+  }
+
+  if (warp < 4) {
+    // ---- producers: 128 x rows and 2*NG W_c rows, 16-byte chunks, 128-byte swizzle ----
+    const int j = tid & 7;
+    const __nv_bfloat16* xs[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = m0 + (tid >> 3) + 16 * i;
+      xs[i] = r < a.R ? a.x + size_t(r) * a.d : nullptr;
+    }
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kCStages;
+      if (it >= kCStages && !mbar_wait(&empty_bar[s], ((it / kCStages) - 1) & 1))
+        record_error(a.err, kDevErrConv);
+      const int kc = (kb0 + it) * kCBK + j * 8;  // first column of this thread's chunk
+      const bool kok = kc < a.d;
+      uint8_t* dA = sA + size_t(s) * kCAStage;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = (tid >> 3) + 16 * i;
+        const bool ok = kok && xs[i] != nullptr;
+        cp_async16(dA + r * 128 + ((j ^ (r & 7)) << 4), ok ? xs[i] + kc : a.x, ok);
+      }
+      uint8_t* dB = sB + size_t(s) * bst;
+      for (int r = tid >> 3; r < N; r += 16) {
+        const int g = g0 + (r < NG ? r : r - NG);
+        const int wrow = (r < NG ? 0 : a.G) + g;
+        const bool ok = kok && g < a.G;
+        cp_async16(dB + r * 128 + ((j ^ (r & 7)) << 4),
+                   ok ? a.W_c + size_t(wrow) * a.d + kc : a.W_c, ok);
+      }
+      cp_async_commit();
+      if (it >= 2) {
+        cp_async_wait<2>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full_bar[(it - 2) % kCStages]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int it = max(0, nkb - 2); it < nkb; ++it) mbar_arrive(&full_bar[it % kCStages]);
+  } else {
+    if (warp == 4 && lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kCBM, N);
+      for (int it = 0; it < nkb; ++it) {
+        const int s = it % kCStages;
+        if (!mbar_wait(&full_bar[s], (it / kCStages) & 1)) record_error(a.err, kDevErrConv);
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kCAStage);
+        const uint64_t bd = umma_desc_sw128(sB + size_t(s) * bst);
+#pragma unroll
+        for (int k = 0; k < kCBK / 16; ++k)
+          umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[s]);
+      }
+      umma_commit(accum_bar);
+    }
+    __syncwarp();
+    // ---- TMEM -> shared memory (the tile's corrections, or this split's partial) ----
+    const int quarter = warp & 3;
+    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+    tc_fence_after();
+    const int lrow = quarter * 32 + lane;
+    float* dst = (a.splits == 1 ? corr : part) + size_t(lrow) * pitch;
+    for (int c = 0; c < N; c += 32) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(dst + c + 4 * q) =
+            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
   }
-  if (!mbar_wait(bar, 0)) record_error(a.err, kDevErrConv);
+  tc_fence_before();
+  int r_lo = 0, r_n = kCBM;
+  if (a.splits == 1) {
+    __syncthreads();
+  } else {
+    // ---- sum the cluster's partials for this CTA's slice of rows (rank order) ----
+    cluster_sync_all();
+    const int S = a.splits;
+    const int per = (kCBM + S - 1) / S;
+    r_lo = split * per;
+    r_n = max(0, min(per, kCBM - r_lo));
+    const int valid = max(0, min(r_n, a.R - (m0 + r_lo)));
+    const int n4 = N / 4;
+    for (int e = tid; e < valid * n4; e += kCThreads) {
+      const int lr = e / n4, c4 = e % n4;
+      const float* src = part + size_t(r_lo + lr) * pitch + 4 * c4;
+      float4 v[kCMaxSplits];
+#pragma unroll
+      for (int k = 0; k < kCMaxSplits; ++k)
+        v[k] = k < S ? dsmem_ld4(dsmem_addr(src, k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 acc = v[0];
+#pragma unroll
+      for (int k = 1; k < kCMaxSplits; ++k) {
+        acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+      }
+      *reinterpret_cast<float4*>(corr + size_t(lr) * pitch + 4 * c4) = acc;
+    }
+    __syncthreads();
+  }
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  pdl_launch_dependents();
 
-  // Corrections: warps split the rows; with fewer rows than warps they also split K.
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // rows >= 8: warp w owns rows w, w+8, ... over all of K.
-  // rows <  8: warp w owns row w % rows over K part w / rows (ksplit parts).
-  const int ksplit = rows >= kConvWarps ? 1 : kConvWarps / rows;
-  const int kpart = ksplit == 1 ? 0 : warp / rows;
-  const int kchunk = (vec_per_row + ksplit - 1) / ksplit;
-  for (int lr = (ksplit == 1 ? warp : warp % rows); lr < rows;
-       lr += (ksplit == 1 ? kConvWarps : rows)) {
-    const int tap = lr / NG, gl = lr % NG;
-    float acc[kMaxTL];
+  // ---- the 2-tap mix: one (row, group) = 16 channels per item, 4 items per pass ----
+  constexpr int kBatch = 4;
+  const int items = r_n * NG;
+  for (int e0 = tid; e0 < items; e0 += kCThreads * kBatch) {
+    uint4 vt[kBatch][2], vm[kBatch][2];
+    bool ok[kBatch];
 #pragma unroll
-    for (int tt = 0; tt < kMaxTL; ++tt) acc[tt] = 0.f;
-    if (gl < ng) {
-      const uint4* wrow = reinterpret_cast<const uint4*>(a.W_c + (size_t(tap) * G + g0 + gl) * d);
-      const int v_lo = kpart * kchunk;
-      const int v_hi = min(vec_per_row, v_lo + kchunk);
-#pragma unroll 4
-      for (int v = v_lo + lane; v < v_hi; v += 32) {
-        const uint4 w = __ldg(wrow + v);
-#pragma unroll
-        for (int tt = 0; tt < kMaxTL; ++tt)
-          if (tt < tl)
-            acc[tt] += dot8(w, reinterpret_cast<const uint4*>(xs + size_t(tt + 1) * d)[v]);
+    for (int u = 0; u < kBatch; ++u) {  // every load of the pass first
+      const int e = e0 + u * kCThreads;
+      const int lr = e / NG, gl = e % NG;
+      const int r = m0 + r_lo + lr, g = g0 + gl;
+      ok[u] = e < items && r < a.R && g < a.G;
+      if (ok[u]) {
+        const int t = r % a.L;
+        const uint4* xt = reinterpret_cast<const uint4*>(a.x + size_t(r) * a.d + 16 * g);
+        const uint4* xm = reinterpret_cast<const uint4*>(
+            (t > 0 ? a.x + size_t(r - 1) * a.d : a.x_prev + size_t(r / a.L) * a.d) + 16 * g);
+        vt[u][0] = xt[0];
+        vt[u][1] = xt[1];
+        vm[u][0] = xm[0];
+        vm[u][1] = xm[1];
       }
     }
 #pragma unroll
-    for (int tt = 0; tt < kMaxTL; ++tt) {
-      float v = acc[tt];
+    for (int u = 0; u < kBatch; ++u) {
+      if (!ok[u]) continue;
+      const int e = e0 + u * kCThreads;
+      const int lr = e / NG, gl = e % NG;
+      const int r = m0 + r_lo + lr, g = g0 + gl;
+      const float c0 = corr[size_t(lr) * pitch + gl];
+      const float c1 = corr[size_t(lr) * pitch + NG + gl];
+      const float* b0 = bslice + 16 * gl;
+      const float* b1 = bslice + 16 * NG + 16 * gl;
+      uint4 out[2];
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-      if (lane == 0 && tt < TL) red[(size_t(kpart) * rows + lr) * TL + tt] = v;
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t tw[4] = {vt[u][h].x, vt[u][h].y, vt[u][h].z, vt[u][h].w};
+        const uint32_t mw[4] = {vm[u][h].x, vm[u][h].y, vm[u][h].z, vm[u][h].w};
+        uint32_t ow[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int ch = 8 * h + 2 * q;
+          const float lo = fmaf(b0[ch] + c0, __uint_as_float(tw[q] << 16),
+                                (b1[ch] + c1) * __uint_as_float(mw[q] << 16));
+          const float hi = fmaf(b0[ch + 1] + c0, __uint_as_float(tw[q] & 0xFFFF0000u),
+                                (b1[ch + 1] + c1) * __uint_as_float(mw[q] & 0xFFFF0000u));
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+          ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
+        }
+        out[h] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      }
+      uint4* yo = reinterpret_cast<uint4*>(a.y + size_t(r) * a.d + 16 * g);
+      yo[0] = out[0];
+      yo[1] = out[1];
     }
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < rows * TL; e += kConvThreads) {
-    float s = 0.f;
-    for (int k = 0; k < ksplit; ++k) s += red[size_t(k) * rows * TL + e];
-    corr[e] = s;
-  }
-  __syncthreads();
-  pdl_launch_dependents();
-
-  // y for the ng*16 channels of this CTA.
-  const int nch = ng * kGroup;
-  for (int e = threadIdx.x; e < tl * nch; e += kConvThreads) {
-    const int tt = e / nch, cl = e % nch;
-    const int c = g0 * kGroup + cl, gl = cl / kGroup;
-    const float k0 = a.base[c] + corr[size_t(gl) * TL + tt];
-    const float k1 = a.base[d + c] + corr[size_t(NG + gl) * TL + tt];
-    const float xt = __bfloat162float(xs[size_t(tt + 1) * d + c]);
-    const float xm1 = __bfloat162float(xs[size_t(tt) * d + c]);
-    const float v = fmaf(k0, xt, k1 * xm1);
-    a.y[(size_t(b) * a.L + t0 + tt) * d + c] = __float2bfloat16_rn(v);
-  }
+  if (a.splits > 1) cluster_sync_all();  // peers may still be reading this CTA's partial
 }
 
-size_t conv_smem_bytes(int TL, int NG, int d) {
-  return size_t(TL + 1) * d * 2 + size_t(kConvWarps + 1) * 2 * NG * TL * sizeof(float) + 16;
-}
-
-bool g_conv_attr_set[64];
+bool g_conv_attr[64];
 
 }  // namespace
 
@@ -146,23 +271,40 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (!g_conv_attr_set[dev & 63]) {
-    e = cudaFuncSetAttribute(conv2_fma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             200 * 1024);
+  if (!g_conv_attr[dev & 63]) {
+    e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(conv_smem_bytes(kCMaxNG)));
     if (e != cudaSuccess) return e;
-    g_conv_attr_set[dev & 63] = true;
+    g_conv_attr[dev & 63] = true;
   }
-  const int G = d / kGroup;
-  int TL = static_cast<int>(kConvXBudget / (size_t(d) * 2)) - 1;
-  TL = max(1, min(TL, min(L, kMaxTL)));
-  const int tiles = (L + TL - 1) / TL;
   const int sms = device_info().sms;
-  int NG = kMaxNG;
-  while (NG > 1 && (long long)((G + NG - 1) / NG) * tiles * B < 2LL * sms) NG >>= 1;
-  ConvArgs a{x, x_prev, base, W_c, y, L, d, G, TL, NG, device_error_word()};
-  const dim3 grid((G + NG - 1) / NG, tiles, B);
-  return launch_k(conv2_fma_kernel, grid, dim3(kConvThreads), conv_smem_bytes(TL, NG, d), s,
-                  false, a);
+  ConvArgs a{};
+  a.x = x;
+  a.x_prev = x_prev;
+  a.base = base;
+  a.W_c = W_c;
+  a.y = y;
+  a.R = B * L;
+  a.L = L;
+  a.d = d;
+  a.G = d / kGroup;
+  a.kblocks = (d + kCBK - 1) / kCBK;
+  a.err = device_error_word();
+  const int mtiles = (a.R + kCBM - 1) / kCBM;
+  // Widest group slice that still gives a full wave of tiles; otherwise the
+  // narrowest slice, with K split over a cluster until the GPU is covered.
+  int NG = kCMaxNG;
+  while (NG > 16 && (long long)mtiles * ((a.G + NG - 1) / NG) < sms) NG >>= 1;
+  a.NG = NG;
+  a.ntiles = (a.G + NG - 1) / NG;
+  const int tiles = mtiles * a.ntiles;
+  int want = 1;
+  while (want * 2 <= kCMaxSplits && tiles * want * 2 <= sms) want *= 2;
+  want = std::min(want, a.kblocks);
+  a.kps = (a.kblocks + want - 1) / want;
+  a.splits = (a.kblocks + a.kps - 1) / a.kps;  // every split gets at least one K block
+  return launch_kc(conv_tc_kernel, dim3(tiles * a.splits), dim3(kCThreads),
+                   conv_smem_bytes(NG), s, false, a.splits, a);
 }
 
 }  // namespace dfl2

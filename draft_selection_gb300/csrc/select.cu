@@ -216,20 +216,24 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tmem_dealloc(tmem, kTmemCols);
   }
   const int S = a.splits;
-  const int rows_per = kBM / S;
+  const int rows_per = (kBM + S - 1) / S;
   const int r0 = split * rows_per;
-  const int n4 = rows_per * (kBN / 4);
   const float* red_base = reinterpret_cast<const float*>(smem);
-  for (int e = tid; e < n4; e += kGemmThreads) {
+  // Only rows that exist are reduced; every peer's value is requested before any is summed.
+  const int valid_rows = max(0, min(min(rows_per, kBM - r0), P.M - (m0 + r0)));
+  for (int e = tid; e < valid_rows * (kBN / 4); e += kGemmThreads) {
     const int lr = r0 + e / (kBN / 4), c4 = e % (kBN / 4);
     const float* src = red_base + size_t(lr) * kRedPitch + c4 * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int k = 0; k < S; ++k) {  // rank order: deterministic
-      const float4 v = dsmem_ld4(dsmem_addr(src, k));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    float4 v[kMaxClusterSplits];
+#pragma unroll
+    for (int k = 0; k < kMaxClusterSplits; ++k)
+      v[k] = k < S ? dsmem_ld4(dsmem_addr(src, k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc = v[0];
+#pragma unroll
+    for (int k = 1; k < kMaxClusterSplits; ++k) {  // rank order: deterministic
+      acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
     }
-    const int grow = m0 + lr;
-    if (grow < P.M) reinterpret_cast<float4*>(P.out + size_t(grow) * kBN)[c4] = acc;
+    reinterpret_cast<float4*>(P.out + size_t(m0 + lr) * kBN)[c4] = acc;
   }
   pdl_launch_dependents();
   cluster_sync_all();  // no CTA leaves while others still read its shared memory
@@ -306,10 +310,16 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
   const int i = tid / kCand, j = tid % kCand;
   float s;
   if (i < npred) {
-    s = 0.f;
+    // Four independent partial sums over the quarters of the rank: shorter chains.
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll 8
-    for (int q = 0; q < kRank; ++q) s = fmaf(Gs[i][q], Bsh[j][q], s);
-    s += U[j];
+    for (int q = 0; q < kRank / 4; ++q) {
+      p0 = fmaf(Gs[i][q], Bsh[j][q], p0);
+      p1 = fmaf(Gs[i][q + 64], Bsh[j][q + 64], p1);
+      p2 = fmaf(Gs[i][q + 128], Bsh[j][q + 128], p2);
+      p3 = fmaf(Gs[i][q + 192], Bsh[j][q + 192], p3);
+    }
+    s = ((p0 + p1) + (p2 + p3)) + U[j];
   } else {
     s = -INFINITY;
   }
@@ -330,8 +340,8 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
     float4* qo = reinterpret_cast<float4*>(a.qrows + (size_t(cell) * kCand + tid) * kCand);
 #pragma unroll
     for (int k = 0; k < 4; ++k) qo[k] = make_float4(qv[4 * k], qv[4 * k + 1], qv[4 * k + 2], qv[4 * k + 3]);
+    __threadfence();  // this row's choice and q are visible before the ticket
   }
-  __threadfence();
   __syncthreads();
   if (tid == 0) {
     const uint32_t ticket = atomicInc(&a.tickets[b], static_cast<unsigned>(a.L - 1));
@@ -392,8 +402,8 @@ SelectPlan select_plan(int B, int L, int d) {
   while (splits * 2 <= kMaxClusterSplits && tiles * splits * 2 <= kGemmTargetCtas &&
          splits * 2 <= p.kblocks)
     splits *= 2;
-  p.splits = splits;
   p.kps = (p.kblocks + splits - 1) / splits;
+  p.splits = (p.kblocks + p.kps - 1) / p.kps;  // every split gets at least one K block
   p.PA_off = 256;
   p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
   p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);

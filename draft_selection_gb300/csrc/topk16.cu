@@ -6,19 +6,24 @@
 //   * Persistent grid: the rows*tiles_per_row 8 KB tiles are cut into equal
 //     contiguous shares, one per CTA, so every SM streams the same number of
 //     bytes whatever B*L is (16 rows at batch 1, 4096 at batch 256).
-//   * One producer thread stages tiles into an 8-deep shared-memory ring with
+//   * One producer thread stages tiles into a 7-deep shared-memory ring with
 //     bulk async copies (cp.async.bulk, completion on mbarriers); eight
-//     consumer warps read the tiles from shared memory.
-//   * Each consumer warp keeps an exact top-16 of 64-bit keys
-//     (ordered value << 32 | ~index) in lanes 0..15.  A block of 256 elements
-//     costs one max and one vote when nothing beats the warp's 16th value; the
-//     rare hits are merged with a 32-lane bitonic sort + merge network.  The
-//     value-only fast filter is exact because a warp meets its elements in
-//     increasing index order, so an element equal to the 16th value always
-//     loses the index tie-break.
-//   * Per CTA the 8 warp lists are merged; rows split across CTAs publish
-//     partial lists and the last CTA to arrive (atomicInc ticket, which also
-//     resets itself) merges them.  No CTA ever waits for another.
+//     consumer warps read the tiles from shared memory, two 16-byte vectors
+//     per lane per tile (each warp: two blocks of 32 vectors).
+//   * Bound: the first tiles of each row segment are held while every warp
+//     reduces its block maxima; the 16th largest of those maxima (16 distinct
+//     elements, so no larger than the row's 16th value) becomes the bound T.
+//   * Candidates: every element >= T is appended, as a 64-bit key
+//     (ordered value << 32 | ~index, unique, larger = better), to a shared
+//     candidate buffer with one warp-aggregated atomic; a tile with no such
+//     element costs two packed maxima and one vote per lane.  Past the
+//     buffer's capacity a warp keeps its overflow in an exact per-warp list.
+//   * Selection by rank: each thread counts the keys that beat its key (one
+//     pass over shared memory, stopping at 16) and a key of rank r < 16 writes
+//     itself to slot r.  Keys are unique, so this is the exact top 16 with no
+//     sorting network.  Rows split across CTAs publish partial lists and the
+//     last CTA to arrive (atomicInc ticket, which also resets itself) ranks
+//     them.  No CTA ever waits for another.
 #include <algorithm>
 
 #include "dfl2_internal.cuh"
@@ -29,13 +34,24 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = 8192;
-constexpr int kStages = 8;
+constexpr int kStages = 7;
 constexpr int kMaxGrid = 2048;
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kBlocksPerTile = 2 * kConsumerWarps;  // blocks of 32 vectors (512 bytes)
+// Tiles at the start of each row segment that feed the block-maximum bound;
+// later tiles skip the reduction and the CTA barrier.
+constexpr int kBoundTiles = 3;
+constexpr int kCandCap = 1024;   // candidate keys buffered per row segment
+constexpr int kMinTilesPerCta = 4;
+static_assert(kBoundTiles < kStages, "held bound tiles must leave the ring room to stream");
+constexpr int kConsumers = kConsumerWarps * 32;
+// [stages][full][empty][cand][extra: per-warp overflow lists][res][block maxima][flags]
 constexpr size_t kSmemBytes = size_t(kStages) * kTileBytes + 2 * kStages * sizeof(uint64_t) +
-                              2 * kConsumerWarps * kCand * sizeof(uint64_t) +
-                              (2 + kConsumerWarps) * sizeof(uint32_t);
-constexpr int kMergeBatch = 4;  // partial lists each warp loads at once in the final merge
+                              size_t(kCandCap) * sizeof(uint64_t) +
+                              size_t(kConsumerWarps) * kCand * sizeof(uint64_t) +
+                              kCand * sizeof(uint64_t) +
+                              size_t(kBoundTiles) * kBlocksPerTile * sizeof(float) + 32;
+static_assert(kTileBytes == kBlocksPerTile * 32 * 16, "a tile is one iteration of all warps");
 
 struct TopkArgs {
   const uint8_t* logits;
@@ -127,97 +143,104 @@ __device__ __forceinline__ void unpack(const uint4& q, float (&f)[EPV]) {
   }
 }
 
+__device__ __forceinline__ float warp_max_f(float x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+  return x;
+}
+
+// Maximum of one 16-byte vector, as float.
+template <int EPV>
+__device__ __forceinline__ float vec_max(const uint4& q) {
+  if constexpr (EPV == 4) {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  } else {
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&q.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&q.y);
+    const __nv_bfloat162 c = *reinterpret_cast<const __nv_bfloat162*>(&q.z);
+    const __nv_bfloat162 d = *reinterpret_cast<const __nv_bfloat162*>(&q.w);
+    const __nv_bfloat162 m = __hmax2(__hmax2(a, b), __hmax2(c, d));
+    return fmaxf(__low2float(m), __high2float(m));
+  }
+}
+
 struct WarpTop {
-  uint64_t list;  // lanes 0..15: keys by rank, 0 = empty
-  uint64_t thr;   // the 16th key (0 while fewer than 16 are held)
-  float thr_v;    // its value
+  uint64_t list;  // lanes 0..15: this warp's overflow keys by rank, 0 = empty
+  float bound;    // the segment's bound T
 };
 
-// cta_thr: the best 16th value any warp of this CTA holds for the current row
-// (as an order-preserving uint32, 0 = none yet).  Some warp holds 16 elements
-// at or above it, so an element strictly below it cannot be in the row's top 16.
-template <int EPV>
-__device__ __forceinline__ void process_block(WarpTop& w, const float (&f)[EPV], bool valid,
-                                              uint32_t idx0, int lane, uint32_t* cta_thr,
-                                              uint32_t* warp_v2, int warp) {
-  float m = f[0];
-#pragma unroll
-  for (int e = 1; e < EPV; ++e) m = fmaxf(m, f[e]);
-  const uint32_t shared_o = *reinterpret_cast<volatile uint32_t*>(cta_thr);
-  const float shared_v = shared_o == 0u ? -INFINITY : unord_f32(shared_o);
-  const bool hit = valid && !(m < shared_v) && (w.thr == 0 || m > w.thr_v);
-  if (!__any_sync(kFull, hit)) return;
-  uint32_t pend = 0;
-  if (w.thr == 0) {
-    // Empty list: seed it with the 16 best lane maxima in one sort.
-    uint64_t lm = 0;
-    if (valid) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const uint64_t k = make_key(f[e], idx0 + e);
-        lm = k > lm ? k : lm;
-      }
+// Exact insertion of one key per lane (0 = none) into the warp's list.
+__device__ __forceinline__ void insert_lane_keys(WarpTop& w, uint64_t cand, int lane) {
+  const unsigned who = __ballot_sync(kFull, cand != 0);
+  if (!who) return;
+  if (__popc(who) <= 2) {
+    unsigned rest = who;
+    while (rest) {
+      const int src = __ffs(rest) - 1;
+      rest &= rest - 1;
+      const uint64_t k = shfl64(cand, src);
+      if (k > shfl64(w.list, 15)) w.list = insert_one(w.list, k, lane);
     }
-    const uint64_t srt = warp_sort32_desc(lm, lane);
-    w.list = merge_sorted16(w.list, srt, lane);
-    w.thr = shfl64(w.list, 15);
-    w.thr_v = unord_f32(static_cast<uint32_t>(w.thr >> 32));
-    if (valid) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        const uint64_t k = make_key(f[e], idx0 + e);
-        if (k > w.thr && k != lm && !(f[e] < shared_v)) pend |= 1u << e;
-      }
-    }
-  } else if (valid) {
-#pragma unroll
-    for (int e = 0; e < EPV; ++e)
-      if (make_key(f[e], idx0 + e) > w.thr && !(f[e] < shared_v)) pend |= 1u << e;
+  } else {
+    w.list = merge_sorted16(w.list, warp_sort32_desc(cand, lane), lane);
   }
-  while (true) {
-    const unsigned who = __ballot_sync(kFull, pend != 0);
-    if (!who) break;
-    uint64_t cand = 0;
-    if (pend) {
-      const int e = __ffs(pend) - 1;
-      pend &= pend - 1;
+}
+
+// The lane's elements at or above the bound go to the CTA candidate buffer
+// (or, past its capacity, into the warp's own exact list).
+template <int EPV>
+__device__ __forceinline__ void collect_hits(WarpTop& w, const uint4& qa, const uint4& qb, bool va,
+                                             bool vb, uint32_t idxA, uint32_t idxB, int lane,
+                                             uint64_t* cand, uint32_t* cand_count) {
+  float f[2 * EPV];
+  {
+    float fa[EPV], fb[EPV];
+    unpack<EPV>(qa, fa);
+    unpack<EPV>(qb, fb);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      f[e] = fa[e];
+      f[EPV + e] = fb[e];
+    }
+  }
+  uint32_t mask = 0;
+#pragma unroll
+  for (int e = 0; e < 2 * EPV; ++e)
+    if ((e < EPV ? va : vb) && f[e] >= w.bound) mask |= 1u << e;
+  const int n = __popc(mask);
+  int pre = n;  // inclusive warp scan of the counts
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFull, pre, off);
+    if (lane >= off) pre += o;
+  }
+  const int total = __shfl_sync(kFull, pre, 31);
+  uint32_t base = 0;
+  if (lane == 0) base = atomicAdd(cand_count, static_cast<uint32_t>(total));
+  base = __shfl_sync(kFull, base, 0);
+  uint32_t pos = base + static_cast<uint32_t>(pre - n);
+  uint32_t over = 0;  // elements that did not fit
+#pragma unroll
+  for (int e = 0; e < 2 * EPV; ++e) {
+    if ((mask >> e) & 1u) {
+      const uint64_t k = make_key(f[e], e < EPV ? idxA + e : idxB + (e - EPV));
+      if (pos < kCandCap) cand[pos] = k;
+      else over |= 1u << e;
+      ++pos;
+    }
+  }
+  while (__any_sync(kFull, over != 0)) {  // only once the buffer is full: exact per-warp list
+    uint64_t k = 0;
+    if (over) {
+      const int e = __ffs(over) - 1;
+      over &= over - 1;
       float v = f[0];
 #pragma unroll
-      for (int e2 = 1; e2 < EPV; ++e2) v = (e2 == e) ? f[e2] : v;
-      cand = make_key(v, idx0 + e);
+      for (int e2 = 1; e2 < 2 * EPV; ++e2) v = (e2 == e) ? f[e2] : v;
+      k = make_key(v, e < EPV ? idxA + e : idxB + (e - EPV));
     }
-    if (__popc(who) <= 2) {
-      // Few candidates (the common case once the list is warm): insert each directly.
-      unsigned rest = who;
-      while (rest) {
-        const int src = __ffs(rest) - 1;
-        rest &= rest - 1;
-        const uint64_t k = shfl64(cand, src);
-        if (k > shfl64(w.list, 15)) w.list = insert_one(w.list, k, lane);
-      }
-    } else {
-      cand = warp_sort32_desc(cand, lane);
-      w.list = merge_sorted16(w.list, cand, lane);
-    }
-    w.thr = shfl64(w.list, 15);
-    w.thr_v = unord_f32(static_cast<uint32_t>(w.thr >> 32));
-    if (pend) {
-#pragma unroll
-      for (int e = 0; e < EPV; ++e)
-        if (((pend >> e) & 1u) && !(make_key(f[e], idx0 + e) > w.thr)) pend &= ~(1u << e);
-    }
-  }
-  // Publish a tighter CTA bound: besides this warp's 16th value, the smallest of
-  // the eight warps' 2nd-best values (8 warps x 2 elements at or above it).
-  const uint64_t second = shfl64(w.list, 1);
-  if (lane == 0) {
-    if (second != 0) warp_v2[warp] = static_cast<uint32_t>(second >> 32);
-    uint32_t m2 = 0xFFFFFFFFu;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) m2 = min(m2, *reinterpret_cast<volatile uint32_t*>(&warp_v2[k]));
-    const uint32_t own = w.thr != 0 ? static_cast<uint32_t>(w.thr >> 32) : 0u;
-    const uint32_t bound = max(own, m2);
-    if (bound != 0u) atomicMax(cta_thr, bound);
+    insert_lane_keys(w, k, lane);
   }
 }
 
@@ -228,16 +251,48 @@ __device__ __forceinline__ void write_row(const TopkArgs& a, long long row, uint
   }
 }
 
+// res[r] = the key of rank r (0-based, by descending key) among keys[0..n),
+// for r < 16.  Keys are unique (0 = empty, skipped); res must hold zeros for
+// ranks that no key takes.  All consumer threads call it; no barrier inside.
+__device__ __forceinline__ void rank_select16(const uint64_t* keys, int n, uint64_t* res,
+                                              int tid) {
+  for (int i = tid; i < n; i += kConsumers) {
+    const uint64_t k = keys[i];
+    if (k == 0) continue;
+    int r = 0;
+    int j = 0;
+    for (; j + 8 <= n && r < kCand; j += 8) {
+#pragma unroll
+      for (int u = 0; u < 8; ++u) r += keys[j + u] > k;
+    }
+    for (; j < n && r < kCand; ++j) r += keys[j] > k;
+    if (r < kCand) res[r] = k;
+  }
+}
+
+// The 16th largest of n block maxima (ties ranked by position); -inf if n < 16.
+__device__ __forceinline__ void rank_bound(const float* bm, int n, float* out, int tid) {
+  for (int i = tid; i < n; i += kConsumers) {
+    const float v = bm[i];
+    int r = 0;
+    for (int j = 0; j < n; ++j) r += (bm[j] > v) || (bm[j] == v && j < i);
+    if (r == kCand - 1) *out = v;
+  }
+}
+
 template <int EPV>
-__global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kTileBytes);
   uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* merge_buf = empty_bar + kStages;  // [2][kConsumerWarps][16]
-  uint32_t* cta_thr = reinterpret_cast<uint32_t*>(merge_buf + 2 * kConsumerWarps * kCand);
-  uint32_t* last_flag = cta_thr + 1;
-  uint32_t* warp_v2 = cta_thr + 2;  // [kConsumerWarps] each warp's 2nd-best value, ordered
+  uint64_t* cand = empty_bar + kStages;                          // [kCandCap]
+  uint64_t* extra = cand + kCandCap;                              // [kConsumerWarps][16]
+  uint64_t* res = extra + kConsumerWarps * kCand;                 // [16]
+  float* bmax = reinterpret_cast<float*>(res + kCand);            // [kBoundTiles][16]
+  uint32_t* last_flag = reinterpret_cast<uint32_t*>(bmax + kBoundTiles * kBlocksPerTile);
+  uint32_t* cand_count = last_flag + 1;
+  float* bound_s = reinterpret_cast<float*>(cand_count + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long T = a.total_tiles;
@@ -252,8 +307,8 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
       mbar_init(&empty_bar[s], kConsumerWarps);
     }
     fence_mbar_init();
-    *cta_thr = 0u;
-    for (int k = 0; k < kConsumerWarps; ++k) warp_v2[k] = 0u;
+    *cand_count = 0u;
+    for (int k = 0; k < kCand; ++k) res[k] = 0ull;
   }
   __syncthreads();
   pdl_wait();  // the logits may come from the previous kernel on the stream
@@ -280,7 +335,60 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
   while (g < g1) {
     const long long row = g / tpr;
     const long long seg_end = min(g1, (row + 1) * tpr);
-    WarpTop w{0ull, 0ull, 0.f};
+    WarpTop w{0ull, -INFINITY};
+    const int nbound = static_cast<int>((seg_end - g < kBoundTiles ? seg_end - g : kBoundTiles));
+    // ---- bound: hold the first nbound tiles, rank their block maxima ----
+    uint4 hqa[kBoundTiles], hqb[kBoundTiles];
+    bool hva[kBoundTiles], hvb[kBoundTiles];
+    float hma[kBoundTiles], hmb[kBoundTiles];
+    uint32_t hia[kBoundTiles], hib[kBoundTiles];
+#pragma unroll
+    for (int k = 0; k < kBoundTiles; ++k) {
+      hva[k] = hvb[k] = false;
+      hma[k] = hmb[k] = -INFINITY;
+      hqa[k] = hqb[k] = make_uint4(0u, 0u, 0u, 0u);
+      hia[k] = hib[k] = 0u;
+      if (k < nbound) {
+        const int s = (i + k) % kStages;
+        if (!mbar_wait(&full_bar[s], ((i + k) / kStages) & 1)) record_error(a.err, kDevErrTopkFull);
+        const int t = static_cast<int>((g + k) % tpr);
+        const int nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
+        const uint32_t elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
+        const uint4* tile = reinterpret_cast<const uint4*>(stages + size_t(s) * kTileBytes);
+        const int v_a = warp * 64 + lane, v_b = v_a + 32;
+        hva[k] = v_a < nvec;
+        hvb[k] = v_b < nvec;
+        if (hva[k]) hqa[k] = tile[v_a];
+        if (hvb[k]) hqb[k] = tile[v_b];
+        hma[k] = hva[k] ? vec_max<EPV>(hqa[k]) : -INFINITY;
+        hmb[k] = hvb[k] ? vec_max<EPV>(hqb[k]) : -INFINITY;
+        hia[k] = elem_base + static_cast<uint32_t>(v_a) * EPV;
+        hib[k] = elem_base + static_cast<uint32_t>(v_b) * EPV;
+        const float bma = warp_max_f(hma[k]), bmb = warp_max_f(hmb[k]);
+        if (lane == 0) {
+          bmax[k * kBlocksPerTile + 2 * warp] = bma;
+          bmax[k * kBlocksPerTile + 2 * warp + 1] = bmb;
+        }
+      }
+    }
+    if (threadIdx.x == 0) *bound_s = -INFINITY;  // read last at the previous segment's start
+    named_sync(1, kConsumers);
+    rank_bound(bmax, nbound * kBlocksPerTile, bound_s, threadIdx.x);
+    named_sync(1, kConsumers);
+    w.bound = *bound_s;
+#pragma unroll
+    for (int k = 0; k < kBoundTiles; ++k) {
+      if (k < nbound) {
+        if (__any_sync(kFull, (hva[k] && hma[k] >= w.bound) || (hvb[k] && hmb[k] >= w.bound)))
+          collect_hits<EPV>(w, hqa[k], hqb[k], hva[k], hvb[k], hia[k], hib[k], lane, cand,
+                            cand_count);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[(i + k) % kStages]);
+      }
+    }
+    g += nbound;
+    i += nbound;
+    // ---- stream the rest of the segment against the bound ----
     for (; g < seg_end; ++g, ++i) {
       const int s = i % kStages;
       if (!mbar_wait(&full_bar[s], (i / kStages) & 1)) record_error(a.err, kDevErrTopkFull);
@@ -289,31 +397,37 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
       const int nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - off) / 16);
       const uint32_t elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
       const uint4* tile = reinterpret_cast<const uint4*>(stages + size_t(s) * kTileBytes);
-      for (int v0 = warp * 32; v0 < nvec; v0 += kConsumerWarps * 32) {
-        const int v = v0 + lane;
-        const bool valid = v < nvec;
-        uint4 q = valid ? tile[v] : make_uint4(0u, 0u, 0u, 0u);
-        float f[EPV];
-        unpack<EPV>(q, f);
-        process_block<EPV>(w, f, valid, elem_base + static_cast<uint32_t>(v) * EPV, lane,
-                           cta_thr, warp_v2, warp);
-      }
+      const int v_a = warp * 64 + lane, v_b = v_a + 32;
+      const bool ok_a = v_a < nvec, ok_b = v_b < nvec;
+      const uint4 qa = ok_a ? tile[v_a] : make_uint4(0u, 0u, 0u, 0u);
+      const uint4 qb = ok_b ? tile[v_b] : make_uint4(0u, 0u, 0u, 0u);
+      const float ma = ok_a ? vec_max<EPV>(qa) : -INFINITY;
+      const float mb = ok_b ? vec_max<EPV>(qb) : -INFINITY;
+      if (__any_sync(kFull, (ok_a && ma >= w.bound) || (ok_b && mb >= w.bound)))
+        collect_hits<EPV>(w, qa, qb, ok_a, ok_b, elem_base + static_cast<uint32_t>(v_a) * EPV,
+                          elem_base + static_cast<uint32_t>(v_b) * EPV, lane, cand, cand_count);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty_bar[s]);
     }
 
-    // Merge the warps' lists for this row segment.
-    uint64_t* mb = merge_buf + (seg & 1) * kConsumerWarps * kCand;
-    if (lane < kCand) mb[warp * kCand + lane] = w.list;
+    // ---- the segment's top 16 by rank over the candidates (+ overflow lists) ----
+    if (lane < kCand) extra[warp * kCand + lane] = w.list;
+    named_sync(1, kConsumers);
+    const uint32_t cnt = *reinterpret_cast<volatile uint32_t*>(cand_count);
+    const int ncand = static_cast<int>(min(cnt, static_cast<uint32_t>(kCandCap)));
+    // The overflow lists sit right after the buffer, so one ranking covers both.
+    if (cnt > static_cast<uint32_t>(kCandCap)) {
+      rank_select16(cand, kCandCap + kConsumerWarps * kCand, res, threadIdx.x);
+    } else {
+      rank_select16(cand, ncand, res, threadIdx.x);
+    }
     const int c_first = owner_cta(row * tpr, T, G);
     const int c_last = owner_cta(row * tpr + tpr - 1, T, G);
     const int ncontrib = c_last - c_first + 1;
     uint64_t* part = a.partial + size_t(row) * a.max_contrib * kCand;
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, kConsumers);
     if (warp == 0) {
-      uint64_t x = w.list;
-      for (int w2 = 1; w2 < kConsumerWarps; ++w2)
-        x = warp_merge32_desc(lane < 16 ? x : mb[w2 * kCand + ((31 - lane) & 15)], lane);
+      const uint64_t x = lane < kCand ? res[lane] : 0ull;
       uint32_t last = 0;
       if (ncontrib == 1) {
         write_row(a, row, x, lane);
@@ -325,39 +439,35 @@ __global__ void __launch_bounds__(kThreads) topk16_kernel(TopkArgs a) {
         if (lane == 0) ticket = atomicInc(&a.tickets[row], static_cast<unsigned>(ncontrib - 1));
         last = __shfl_sync(kFull, ticket, 0) == static_cast<uint32_t>(ncontrib - 1);
       }
+      if (lane < kCand) res[lane] = 0ull;
       if (lane == 0) {
         *last_flag = last;
-        *cta_thr = 0u;  // the next segment is another row
-        for (int k = 0; k < kConsumerWarps; ++k) warp_v2[k] = 0u;
+        *cand_count = 0u;  // every warp has read it before the barrier above
       }
     }
-    named_sync(1, kConsumerWarps * 32);
+    named_sync(1, kConsumers);
     if (*last_flag) {
-      // Last CTA of a split row: every warp merges a share of the partial lists,
-      // loading kMergeBatch lists at a time, then warp 0 merges the warps' results.
+      // Last CTA of a split row: rank the partial lists, kCandCap - 16 keys at a
+      // time, carrying the running top 16 in front of each batch.
       __threadfence();
       const unsigned long long* pp = reinterpret_cast<const unsigned long long*>(part);
-      uint64_t acc = 0;
-      for (int k0 = warp; k0 < ncontrib; k0 += kConsumerWarps * kMergeBatch) {
-        uint64_t y[kMergeBatch];
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) {
-          const int k = k0 + u * kConsumerWarps;
-          y[u] = k < ncontrib ? __ldcg(pp + k * kCand + ((31 - lane) & 15)) : 0ull;
-        }
-#pragma unroll
-        for (int u = 0; u < kMergeBatch; ++u) acc = warp_merge32_desc(lane < 16 ? acc : y[u], lane);
+      const int total = ncontrib * kCand;
+      constexpr int kBatchKeys = kCandCap - kCand;
+      for (int b0 = 0; b0 < total; b0 += kBatchKeys) {
+        const int nb = min(kBatchKeys, total - b0);
+        for (int e = threadIdx.x; e < nb; e += kConsumers) cand[kCand + e] = __ldcg(pp + b0 + e);
+        if (threadIdx.x < kCand) cand[threadIdx.x] = res[threadIdx.x];
+        named_sync(1, kConsumers);
+        if (threadIdx.x < kCand) res[threadIdx.x] = 0ull;
+        named_sync(1, kConsumers);
+        rank_select16(cand, kCand + nb, res, threadIdx.x);
+        named_sync(1, kConsumers);
       }
-      uint64_t* mb2 = merge_buf + ((seg + 1) & 1) * kConsumerWarps * kCand;
-      if (lane < kCand) mb2[warp * kCand + lane] = acc;
-      named_sync(1, kConsumerWarps * 32);
       if (warp == 0) {
-        uint64_t x = acc;
-        for (int w2 = 1; w2 < kConsumerWarps; ++w2)
-          x = warp_merge32_desc(lane < 16 ? x : mb2[w2 * kCand + ((31 - lane) & 15)], lane);
-        write_row(a, row, x, lane);
+        write_row(a, row, lane < kCand ? res[lane] : 0ull, lane);
+        if (lane < kCand) res[lane] = 0ull;
       }
-      named_sync(1, kConsumerWarps * 32);
+      named_sync(1, kConsumers);
     }
     ++seg;
   }
@@ -423,7 +533,11 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
   const DeviceInfo info = device_info();
   const int occ = plan.elem_bytes == 4 ? k->occ4 : k->occ2;
   const long long T = (long long)plan.rows * plan.tiles_per_row;
-  const int grid = static_cast<int>(std::min<long long>(T, std::min(kMaxGrid, info.sms * std::max(occ, 1))));
+  // One wave of resident CTAs, but no fewer than kMinTilesPerCta tiles per CTA
+  // while that still puts one CTA on every SM (fewer partial lists per row).
+  long long grid_l = std::min<long long>(kMaxGrid, (long long)info.sms * std::max(occ, 1));
+  grid_l = std::min(grid_l, std::max<long long>(info.sms, (T + kMinTilesPerCta - 1) / kMinTilesPerCta));
+  const int grid = static_cast<int>(std::min<long long>(T, grid_l));
   TopkArgs a;
   a.logits = static_cast<const uint8_t*>(logits);
   a.V = plan.V;
