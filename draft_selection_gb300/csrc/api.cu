@@ -285,7 +285,7 @@ dfl2_status dfl2_topk(const void* logits, dfl2_dtype dtype, int B, int L, int V,
   DFL2_TRY(check_device(ptrs));
   DFL2_TRY(check_device_ptr(ws, "workspace"));
   cudaError_t e = dfl2::launch_topk(plan, logits, cand_idx, cand_val, ws,
-                                    reinterpret_cast<cudaStream_t>(stream), false);
+                                    reinterpret_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return cuda_fail(e, "top-16 launch");
   return DFL2_OK;
 }
@@ -312,7 +312,7 @@ dfl2_status dfl2_select(const int32_t* cand_idx, const float* cand_val,
   DFL2_TRY(check_device_ptr(ws, "workspace"));
   cudaError_t e = dfl2::launch_select(plan, cand_idx, cand_val, verified_tok, bf(hidden), bf(E),
                                       bf(W_A), bf(W_B), bf(W_H), V, scores, nullptr, ws,
-                                      reinterpret_cast<cudaStream_t>(stream), false);
+                                      reinterpret_cast<cudaStream_t>(stream), true);
   if (e != cudaSuccess) return cuda_fail(e, "selector launch");
   return DFL2_OK;
 }
@@ -331,7 +331,7 @@ dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L
   DFL2_TRY(check_device(ptrs));
   cudaError_t e = dfl2::launch_walk(scores, cand_idx, B, L, temperature, seeds, cycle_offset,
                                     tokens, slots, q, reinterpret_cast<cudaStream_t>(stream),
-                                    false);
+                                    true);
   if (e != cudaSuccess) return cuda_fail(e, "walk launch");
   return DFL2_OK;
 }
@@ -389,7 +389,7 @@ dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verif
   float* val = cand_val ? cand_val : reinterpret_cast<float*>(w + t.val_off);
   float* S = scores ? scores : reinterpret_cast<float*>(w + t.scores_off);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dfl2::launch_topk(t.topk, logits, idx, val, w + t.topk_off, s, false);
+  cudaError_t e = dfl2::launch_topk(t.topk, logits, idx, val, w + t.topk_off, s, true);
   if (e != cudaSuccess) return cuda_fail(e, "top-16 launch");
   const dfl2::WalkFuse wf{temperature, seeds, cycle_offset, tokens, slots, q};
   e = dfl2::launch_select(t.sel, idx, val, verified_tok, bf(hidden), bf(E), bf(W_A), bf(W_B),

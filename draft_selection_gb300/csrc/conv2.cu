@@ -13,6 +13,14 @@
 // bf16: the corrections never leave the chip.  With few positions (batch 1),
 // K is split over a thread-block cluster and the partial corrections are summed
 // through distributed shared memory, each CTA then mixing its slice of rows.
+//
+// For few positions (R <= 64, batch 1) a transposed kernel computes
+// corr^T = W_sel x^T instead: the 128 W_c rows of 64 groups (both taps) are the
+// A operand, loaded by TMA with no padding, and the R positions are N.  K is
+// split over a cluster; each CTA pushes its small partial (128 x R) to the CTA
+// that owns those groups, which sums the splits in rank order and mixes.
+#include <cuda.h>
+
 #include <algorithm>
 
 #include "dfl2_internal.cuh"
@@ -20,7 +28,8 @@
 namespace dfl2 {
 namespace {
 
-constexpr int kCBM = 128, kCBK = 64, kCStages = 4, kCThreads = 256;
+constexpr int kCBM = 128, kCBK = 64, kCThreads = 256;
+constexpr int kCMaxStages = 4;
 constexpr int kCMaxNG = 64;          // groups per CTA: N = 2*NG <= 128
 constexpr int kCMaxSplits = 8;       // portable cluster size
 constexpr int kCAStage = kCBM * kCBK * 2;  // 16 KB
@@ -32,22 +41,28 @@ struct ConvArgs {
   const __nv_bfloat16* W_c;     // [2G, d]
   __nv_bfloat16* y;             // [R, d]
   int R, L, d, G;
-  int NG, ntiles, splits, kps, kblocks;
+  int NG, ntiles, splits, kps, kblocks, stages;
   uint32_t* err;
 };
 
 __host__ __device__ constexpr int conv_bstage_bytes(int NG) { return 2 * NG * kCBK * 2; }
 __host__ __device__ constexpr int conv_pitch(int NG) { return 2 * NG + 4; }  // fp32 per row
 
-__host__ __device__ size_t conv_part_bytes(int NG) { return size_t(kCBM) * conv_pitch(NG) * 4; }
+// Operand stages: as many as fit beside the other regions (more in flight at batch 1).
+__host__ __device__ constexpr int conv_stages(int) { return 4; }
+__host__ __device__ size_t conv_tile_bytes(int NG) { return size_t(kCBM) * conv_pitch(NG) * 4; }
 __host__ __device__ size_t conv_stage_area(int NG) {
-  const size_t stages = size_t(kCStages) * (kCAStage + conv_bstage_bytes(NG));
-  const size_t part = conv_part_bytes(NG);
-  return stages > part ? stages : part;
+  return size_t(conv_stages(NG)) * (kCAStage + conv_bstage_bytes(NG));
+}
+// Receive slots for split K: S slots of ceil(128/S) rows, at most 128 + S rows.
+// K is only split when the narrowest group slice (16) leaves the GPU short of tiles.
+__host__ __device__ size_t conv_recv_bytes(int NG) {
+  return NG == 16 ? size_t(kCBM + kCMaxSplits) * conv_pitch(NG) * 4 : 0;
 }
 size_t conv_smem_bytes(int NG) {
-  // [operand stages | partial tile (reuses them)] [corrections] [base slice] [barriers]
-  return 1024 + conv_stage_area(NG) + conv_part_bytes(NG) + size_t(2) * 16 * NG * 4 + 128;
+  // [operand stages] [corrections] [receive slots] [base slice] [barriers]
+  return 1024 + conv_stage_area(NG) + conv_tile_bytes(NG) + conv_recv_bytes(NG) +
+         size_t(2) * 16 * NG * 4 + 256;
 }
 
 __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constant__ ConvArgs a) {
@@ -56,14 +71,15 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
                                              ~uintptr_t(1023));
   const int NG = a.NG, N = 2 * NG, pitch = conv_pitch(NG);
   const int bst = conv_bstage_bytes(NG);
+  const int kCStages = a.stages;
   uint8_t* sA = smem;
   uint8_t* sB = smem + size_t(kCStages) * kCAStage;
-  float* part = reinterpret_cast<float*>(smem);  // reuses the stages after the mainloop
-  float* corr = reinterpret_cast<float*>(smem + conv_stage_area(NG));
-  float* bslice = corr + size_t(kCBM) * pitch;   // [2][16*NG]
+  float* corr = reinterpret_cast<float*>(smem + conv_stage_area(NG));  // [128][pitch]
+  float* recv = corr + size_t(kCBM) * pitch;                             // [S][rows_per][pitch]
+  float* bslice = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(recv) + conv_recv_bytes(NG));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * NG);
-  uint64_t* empty_bar = full_bar + kCStages;
-  uint64_t* accum_bar = empty_bar + kCStages;
+  uint64_t* empty_bar = full_bar + kCMaxStages;
+  uint64_t* accum_bar = empty_bar + kCMaxStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -89,10 +105,11 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
-  // base slice for the CTA's channels (zero past d)
-  for (int e = tid; e < 2 * 16 * NG; e += kCThreads) {
-    const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
-    bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+  if (warp >= 5) {  // idle during the mainloop: the base slice for the CTA's channels
+    for (int e = tid - 5 * 32; e < 2 * 16 * NG; e += kCThreads - 5 * 32) {
+      const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
+      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+    }
   }
 
   if (warp < 4) {
@@ -152,19 +169,31 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       umma_commit(accum_bar);
     }
     __syncwarp();
-    // ---- TMEM -> shared memory (the tile's corrections, or this split's partial) ----
+    // ---- TMEM -> the corrections (one split), or push this split's partial rows
+    // into the receive slot of the CTA that owns them (split K) ----
     const int quarter = warp & 3;
     if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
     tc_fence_after();
     const int lrow = quarter * 32 + lane;
-    float* dst = (a.splits == 1 ? corr : part) + size_t(lrow) * pitch;
+    const int per = (kCBM + a.splits - 1) / a.splits;
+    const int owner = lrow / per;
+    const bool live = m0 + lrow < a.R;  // rows past R carry nothing
     for (int c = 0; c < N; c += 32) {
       float v[32];
       tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c), v);
+      if (a.splits == 1) {
+        float* dst = corr + size_t(lrow) * pitch + c;
 #pragma unroll
-      for (int q = 0; q < 8; ++q)
-        *reinterpret_cast<float4*>(dst + c + 4 * q) =
-            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(dst + 4 * q) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      } else if (live) {
+        const float* slot = recv + (size_t(split) * per + (lrow - owner * per)) * pitch + c;
+        const uint32_t dst = dsmem_addr(slot, static_cast<uint32_t>(owner));
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          dsmem_st4(dst + 16u * q, make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+      }
     }
   }
   tc_fence_before();
@@ -172,7 +201,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   if (a.splits == 1) {
     __syncthreads();
   } else {
-    // ---- sum the cluster's partials for this CTA's slice of rows (rank order) ----
+    // ---- every slot has arrived: sum this CTA's rows over the splits, in rank order ----
     cluster_sync_all();
     const int S = a.splits;
     const int per = (kCBM + S - 1) / S;
@@ -182,15 +211,10 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
     const int n4 = N / 4;
     for (int e = tid; e < valid * n4; e += kCThreads) {
       const int lr = e / n4, c4 = e % n4;
-      const float* src = part + size_t(r_lo + lr) * pitch + 4 * c4;
-      float4 v[kCMaxSplits];
-#pragma unroll
-      for (int k = 0; k < kCMaxSplits; ++k)
-        v[k] = k < S ? dsmem_ld4(dsmem_addr(src, k)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 acc = v[0];
-#pragma unroll
-      for (int k = 1; k < kCMaxSplits; ++k) {
-        acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+      float4 acc = *reinterpret_cast<const float4*>(recv + size_t(lr) * pitch + 4 * c4);
+      for (int k = 1; k < S; ++k) {
+        const float4 v = *reinterpret_cast<const float4*>(recv + (size_t(k) * per + lr) * pitch + 4 * c4);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
       }
       *reinterpret_cast<float4*>(corr + size_t(lr) * pitch + 4 * c4) = acc;
     }
@@ -258,10 +282,215 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       yo[1] = out[1];
     }
   }
-  if (a.splits > 1) cluster_sync_all();  // peers may still be reading this CTA's partial
 }
 
 bool g_conv_attr[64];
+
+// ============================================================================
+// Few positions: corr^T = W_sel x^T (W_c rows as A, positions as N).
+// ============================================================================
+constexpr int kSStages = 4;
+constexpr int kSGroups = 64;  // groups per CTA tile: 128 W_c rows (both taps)
+constexpr int kSMaxRows = 64; // positions handled by the transposed kernel (N <= 64)
+
+struct ConvSmallArgs {
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* x_prev;
+  const float* base;
+  __nv_bfloat16* y;
+  int R, L, d, G, Npad, splits, kps, kblocks;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr int small_pitch(int Npad) { return Npad + 4; }
+__host__ __device__ size_t small_smem_bytes(int Npad, int S) {
+  const size_t stages = size_t(kSStages) * (kCAStage + size_t(Npad) * 128);
+  const int owned_rows = 2 * (kSGroups / S);
+  const size_t recv = size_t(S) * owned_rows * small_pitch(Npad) * 4;
+  const size_t corr = size_t(owned_rows) * small_pitch(Npad) * 4;
+  const size_t bsl = size_t(2) * 16 * (kSGroups / S) * 4;
+  return 1024 + stages + recv + corr + bsl + 256;
+}
+
+__global__ void __launch_bounds__(kCThreads, 1)
+    conv_small_kernel(const __grid_constant__ ConvSmallArgs a,
+                      const __grid_constant__ CUtensorMap tmW) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int S = a.splits, Np = a.Npad, pitch = small_pitch(Np);
+  const int og = kSGroups / S;    // groups this CTA mixes
+  const int orows = 2 * og;       // their W_c rows (tap 0, then tap 1)
+  uint8_t* sA = smem;                                          // [stages][128 rows][128 B]
+  uint8_t* sB = smem + size_t(kSStages) * kCAStage;            // [stages][Np rows][128 B]
+  float* recv = reinterpret_cast<float*>(sB + size_t(kSStages) * Np * 128);  // [S][orows][pitch]
+  float* corr = recv + size_t(S) * orows * pitch;              // [orows][pitch]
+  float* bslice = corr + size_t(orows) * pitch;                // [2][16*og]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * og);
+  uint64_t* empty_bar = full_bar + kSStages;
+  uint64_t* accum_bar = empty_bar + kSStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % S;
+  const int g0 = (blockIdx.x / S) * kSGroups;
+  const int kb0 = split * a.kps;
+  const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;
+  const uint32_t ncols = Np <= 32 ? 32u : (Np <= 64 ? 64u : 128u);
+  const int gown = g0 + split * og;  // first group this CTA mixes
+
+  if (tid == 0) {
+    for (int st = 0; st < kSStages; ++st) {
+      mbar_init(&full_bar[st], 1 + 32);  // the TMA expect_tx + the 32 lanes staging x
+      mbar_init(&empty_bar[st], 1);
+    }
+    mbar_init(accum_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    // ---- producer: W_c rows by TMA (two boxes of 64 rows), x rows by cp.async ----
+    for (int it = 0; it < nkb; ++it) {
+      const int st = it % kSStages;
+      if (it >= kSStages && !mbar_wait(&empty_bar[st], ((it / kSStages) - 1) & 1))
+        record_error(a.err, kDevErrConv);
+      const int k0 = (kb0 + it) * kCBK;
+      uint8_t* dA = sA + size_t(st) * kCAStage;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full_bar[st], kCAStage);
+        tma_load_2d(dA, &tmW, k0, g0, &full_bar[st]);
+        tma_load_2d(dA + kCAStage / 2, &tmW, k0, a.G + g0, &full_bar[st]);
+      }
+      uint8_t* dB = sB + size_t(st) * Np * 128;
+      for (int ch = lane; ch < Np * 8; ch += 32) {
+        const int r = ch >> 3, j = ch & 7;
+        const bool ok = r < a.R;
+        cp_async16(dB + r * 128 + ((j ^ (r & 7)) << 4),
+                   ok ? a.x + size_t(r) * a.d + k0 + j * 8 : a.x, ok);
+      }
+      cp_async_commit();
+      if (it >= 2) {
+        cp_async_wait<2>();
+        fence_proxy_async_smem();
+        mbar_arrive(&full_bar[(it - 2) % kSStages]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int it = max(0, nkb - 2); it < nkb; ++it) mbar_arrive(&full_bar[it % kSStages]);
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kCBM, Np);
+      for (int it = 0; it < nkb; ++it) {
+        const int st = it % kSStages;
+        if (!mbar_wait(&full_bar[st], (it / kSStages) & 1)) record_error(a.err, kDevErrConv);
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(sA + size_t(st) * kCAStage);
+        const uint64_t bd = umma_desc_sw128(sB + size_t(st) * Np * 128);
+#pragma unroll
+        for (int k = 0; k < kCBK / 16; ++k)
+          umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[st]);
+      }
+      umma_commit(accum_bar);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // idle during the mainloop: the base slice of the channels this CTA mixes
+    for (int e = tid - 64; e < 2 * 16 * og; e += 64) {
+      const int tap = e / (16 * og), c = 16 * gown + e % (16 * og);
+      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+    }
+  } else {
+    // ---- TMEM row r = W_c row (tap r/64, group g0 + r%64), columns = positions:
+    // push the R values to the CTA that mixes that group ----
+    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int tap = r / kSGroups, gl = r % kSGroups;
+    const int owner = gl / og;
+    const int orow = tap * og + (gl % og);
+    const uint32_t dst = dsmem_addr(recv + (size_t(split) * orows + orow) * pitch,
+                                    static_cast<uint32_t>(owner));
+    for (int c = 0; c < Np; c += 32) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c + 4 * q < Np)
+          dsmem_st4(dst + uint32_t(c + 4 * q) * 4u,
+                    make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // all partials have arrived (also a CTA barrier)
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  // ---- sum the splits in rank order for this CTA's rows ----
+  const int n4 = orows * (Np / 4);
+  for (int e = tid; e < n4; e += kCThreads) {
+    const int orow = e / (Np / 4), c4 = e % (Np / 4);
+    float4 acc = *reinterpret_cast<const float4*>(recv + size_t(orow) * pitch + 4 * c4);
+    for (int k = 1; k < S; ++k) {
+      const float4 v = *reinterpret_cast<const float4*>(recv + (size_t(k) * orows + orow) * pitch + 4 * c4);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(corr + size_t(orow) * pitch + 4 * c4) = acc;
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  // ---- the 2-tap mix for the owned groups: one (position, group) per item ----
+  const int items = a.R * og;
+  for (int e = tid; e < items; e += kCThreads) {
+    const int p = e / og, gl = e % og;
+    const int g = gown + gl;
+    if (g >= a.G) continue;
+    const int t = p % a.L;
+    const float c0 = corr[size_t(gl) * pitch + p];
+    const float c1 = corr[size_t(og + gl) * pitch + p];
+    const uint4* xt = reinterpret_cast<const uint4*>(a.x + size_t(p) * a.d + 16 * g);
+    const uint4* xm = reinterpret_cast<const uint4*>(
+        (t > 0 ? a.x + size_t(p - 1) * a.d : a.x_prev + size_t(p / a.L) * a.d) + 16 * g);
+    const uint4 vt0 = xt[0], vt1 = xt[1], vm0 = xm[0], vm1 = xm[1];
+    const float* b0 = bslice + 16 * gl;
+    const float* b1 = bslice + 16 * og + 16 * gl;
+    uint4 out[2];
+    const uint4 vts[2] = {vt0, vt1}, vms[2] = {vm0, vm1};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t tw[4] = {vts[h].x, vts[h].y, vts[h].z, vts[h].w};
+      const uint32_t mw[4] = {vms[h].x, vms[h].y, vms[h].z, vms[h].w};
+      uint32_t ow[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int ch = 8 * h + 2 * q;
+        const float lo = fmaf(b0[ch] + c0, __uint_as_float(tw[q] << 16),
+                              (b1[ch] + c1) * __uint_as_float(mw[q] << 16));
+        const float hi = fmaf(b0[ch + 1] + c0, __uint_as_float(tw[q] & 0xFFFF0000u),
+                              (b1[ch + 1] + c1) * __uint_as_float(mw[q] & 0xFFFF0000u));
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+        ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
+      out[h] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    }
+    uint4* yo = reinterpret_cast<uint4*>(a.y + size_t(p) * a.d + 16 * g);
+    yo[0] = out[0];
+    yo[1] = out[1];
+  }
+}
+
+bool g_conv_small_attr[64];
+
 
 }  // namespace
 
@@ -273,11 +502,47 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   if (e != cudaSuccess) return e;
   if (!g_conv_attr[dev & 63]) {
     e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(conv_smem_bytes(kCMaxNG)));
+                             static_cast<int>(std::max(conv_smem_bytes(16), conv_smem_bytes(kCMaxNG))));
     if (e != cudaSuccess) return e;
     g_conv_attr[dev & 63] = true;
   }
   const int sms = device_info().sms;
+  const int R = B * L;
+  if (R <= kSMaxRows && d % kCBK == 0 && d / kGroup >= kSGroups / 2) {
+    // ---- few positions: the transposed kernel ----
+    if (!g_conv_small_attr[dev & 63]) {
+      e = cudaFuncSetAttribute(conv_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(small_smem_bytes(kSMaxRows, 1)));
+      if (e != cudaSuccess) return e;
+      g_conv_small_attr[dev & 63] = true;
+    }
+    ConvSmallArgs c{};
+    c.x = x;
+    c.x_prev = x_prev;
+    c.base = base;
+    c.y = y;
+    c.R = R;
+    c.L = L;
+    c.d = d;
+    c.G = d / kGroup;
+    c.Npad = (R + 15) / 16 * 16;
+    c.kblocks = d / kCBK;
+    c.err = device_error_word();
+    const int tiles = (c.G + kSGroups - 1) / kSGroups;
+    int want = 1;
+    while (want * 2 <= kCMaxSplits && tiles * want * 2 <= sms && want * 2 <= c.kblocks) want *= 2;
+    c.splits = want;  // a power of two: it divides the 64 groups of a tile
+    c.kps = (c.kblocks + want - 1) / want;
+    if ((c.splits - 1) * c.kps >= c.kblocks) {  // keep every split non-empty
+      while (c.splits > 1 && (c.splits - 1) * c.kps >= c.kblocks) c.splits >>= 1;
+      c.kps = (c.kblocks + c.splits - 1) / c.splits;
+    }
+    alignas(64) CUtensorMap tmW;
+    if (!tensor_map_bf16(W_c, uint64_t(2) * c.G, uint64_t(d), kSGroups, &tmW))
+      return cudaErrorInvalidValue;
+    return launch_kc(conv_small_kernel, dim3(tiles * c.splits), dim3(kCThreads),
+                     small_smem_bytes(c.Npad, c.splits), s, true, c.splits, c, tmW);
+  }
   ConvArgs a{};
   a.x = x;
   a.x_prev = x_prev;
@@ -303,8 +568,10 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   want = std::min(want, a.kblocks);
   a.kps = (a.kblocks + want - 1) / want;
   a.splits = (a.kblocks + a.kps - 1) / a.kps;  // every split gets at least one K block
+  a.stages = conv_stages(NG);
+  if (a.splits > 1 && NG != 16) return cudaErrorInvalidConfiguration;  // receive slots need NG 16
   return launch_kc(conv_tc_kernel, dim3(tiles * a.splits), dim3(kCThreads),
-                   conv_smem_bytes(NG), s, false, a.splits, a);
+                   conv_smem_bytes(NG), s, true, a.splits, a);
 }
 
 }  // namespace dfl2

@@ -146,6 +146,7 @@ struct SelectPlan {
   size_t PA_off;       // float32 [MA][256]
   size_t PB_off;       // float32 [MB][256]
   size_t GH_off;       // float32 [MH][256], before the sigmoid
+  size_t part_off;     // float32 split-K partials [splits][MA|MB|MH][256] (splits > 1)
   size_t ticket_off;   // uint32 [B]: per-sequence tickets of the fused pair + walk kernel
   size_t choice_off;   // int32 [B*L][16]: per-row walk choice
   size_t q_off;        // float32 [B*L][16][16]: per-row draft distribution
@@ -347,6 +348,11 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank)
   uint32_t out;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(local)), "r"(rank));
   return out;
+}
+__device__ __forceinline__ void dsmem_st4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x), "f"(v.y),
+               "f"(v.z), "f"(v.w)
+               : "memory");
 }
 __device__ __forceinline__ float4 dsmem_ld4(uint32_t addr) {
   float4 v;

@@ -39,10 +39,8 @@ constexpr int kBStage = kBN * kBK * 2;  // 32 KB
 constexpr int kGemmThreads = 256;       // warps 0-3 load, warp 4 issues MMAs, warps 4-7 drain TMEM
 constexpr int kGemmTargetCtas = 148;
 constexpr int kMaxClusterSplits = 8;       // portable cluster size
-constexpr int kRedPitch = kBN + 4;         // fp32 row pitch of the on-chip partial tile
 constexpr size_t kGemmSmem = 1024 + size_t(kGStages) * (kAStage + kBStage) + 256;
-static_assert(size_t(kBM) * kRedPitch * 4 <= size_t(kGStages) * (kAStage + kBStage),
-              "the partial tile reuses the operand stages");
+
 constexpr uint32_t kTmemCols = 256;
 
 enum RowKind : int { kRowsPA = 0, kRowsPB = 1, kRowsHidden = 2 };
@@ -52,6 +50,7 @@ struct GemmProblem {
   int M;        // rows
   int mtiles;   // ceil(M / 128)
   float* out;   // [M][256]
+  float* part;  // [splits][M][256] split-K partials (split K only)
 };
 
 struct GemmArgs {
@@ -178,24 +177,22 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       umma_commit(accum_bar);
     }
     __syncwarp();
-    // ---- epilogue: TMEM -> registers -> global (one split) or own smem (cluster) ----
-    const int quarter = warp & 3;
     if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrGemm);
     tc_fence_after();
-    const int lrow = quarter * 32 + lane;
-    const int row = m0 + lrow;
-    float* red = reinterpret_cast<float*>(smem) + size_t(lrow) * kRedPitch;
+    if (a.splits == 1) {
+      // ---- one split: TMEM -> registers -> the output rows ----
+      const int quarter = warp & 3;
+      const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
-      float v[32];
-      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
-      float4* o = a.splits == 1 ? (row < P.M ? reinterpret_cast<float4*>(P.out + size_t(row) * kBN + c * 32)
-                                             : nullptr)
-                                : reinterpret_cast<float4*>(red + c * 32);
-      if (o) {
+      for (int c = 0; c < kBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
+        if (row < P.M) {
+          float4* o = reinterpret_cast<float4*>(P.out + size_t(row) * kBN + c * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int q = 0; q < 8; ++q)
+            o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
       }
     }
   }
@@ -209,34 +206,53 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     return;
   }
-  // ---- split K: reduce the cluster's partial tiles through distributed smem ----
-  cluster_sync_all();  // every CTA's partial tile is complete (also a CTA barrier)
+  // ---- split K over the cluster: every CTA stores its fp32 partial tile to the
+  // workspace (L2), then each CTA sums one slice of rows over the splits in rank
+  // order (deterministic) and writes the result ----
+  const int S = a.splits;
+  float* mypart = P.part + (size_t(split) * P.M) * kBN;
+  if (warp >= 4) {
+    const int quarter = warp & 3;
+    const int row = m0 + quarter * 32 + lane;
+#pragma unroll 1
+    for (int c = 0; c < kBN / 32; ++c) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
+      if (row < P.M) {
+        float4* o = reinterpret_cast<float4*>(mypart + size_t(row) * kBN + c * 32);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every split's partial tile is in the workspace
   if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  const int S = a.splits;
-  const int rows_per = (kBM + S - 1) / S;
-  const int r0 = split * rows_per;
-  const float* red_base = reinterpret_cast<const float*>(smem);
-  // Only rows that exist are reduced; every peer's value is requested before any is summed.
-  const int valid_rows = max(0, min(min(rows_per, kBM - r0), P.M - (m0 + r0)));
-  for (int e = tid; e < valid_rows * (kBN / 4); e += kGemmThreads) {
-    const int lr = r0 + e / (kBN / 4), c4 = e % (kBN / 4);
-    const float* src = red_base + size_t(lr) * kRedPitch + c4 * 4;
-    float4 v[kMaxClusterSplits];
+  const int per = (kBM + S - 1) / S;
+  const int r0 = split * per;
+  const int valid_rows = max(0, min(min(per, kBM - r0), P.M - (m0 + r0)));
+  const int n4 = valid_rows * (kBN / 4);
+  constexpr int kMaxSplitLoads = kMaxClusterSplits;
+  for (int e = tid; e < n4; e += kGemmThreads) {
+    const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
+    const size_t at = size_t(m0 + r0 + lr) * kBN + 4 * c4;
+    float4 v[kMaxSplitLoads];
 #pragma unroll
-    for (int k = 0; k < kMaxClusterSplits; ++k)
-      v[k] = k < S ? dsmem_ld4(dsmem_addr(src, k)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < kMaxSplitLoads; ++k)  // every split's value requested first
+      v[k] = k < S ? __ldcg(reinterpret_cast<const float4*>(P.part + size_t(k) * P.M * kBN + at))
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
     float4 acc = v[0];
 #pragma unroll
-    for (int k = 1; k < kMaxClusterSplits; ++k) {  // rank order: deterministic
+    for (int k = 1; k < kMaxSplitLoads; ++k) {  // rank order: deterministic
       acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
     }
-    reinterpret_cast<float4*>(P.out + size_t(m0 + lr) * kBN)[c4] = acc;
+    *reinterpret_cast<float4*>(P.out + at) = acc;
   }
   pdl_launch_dependents();
-  cluster_sync_all();  // no CTA leaves while others still read its shared memory
 }
 
 struct PairArgs {
@@ -407,7 +423,9 @@ SelectPlan select_plan(int B, int L, int d) {
   p.PA_off = 256;
   p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
   p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);
-  p.ticket_off = align_up(p.GH_off + size_t(p.MH) * kRank * 4, 256);
+  p.part_off = align_up(p.GH_off + size_t(p.MH) * kRank * 4, 256);
+  const size_t part_bytes = p.splits > 1 ? size_t(p.splits) * (p.MA + p.MB + p.MH) * kRank * 4 : 0;
+  p.ticket_off = align_up(p.part_off + part_bytes, 256);
   p.choice_off = align_up(p.ticket_off + size_t(B) * 4, 256);
   p.q_off = align_up(p.choice_off + size_t(B) * L * kCand * 4, 256);
   p.ws_bytes = align_up(p.q_off + size_t(B) * L * kCand * kCand * 4, 256);
@@ -441,12 +459,15 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   GemmArgs g{};
   const int Ms[3] = {p.MA, p.MB, p.MH};
   float* outs[3] = {PA, PB, GH};
+  float* part = reinterpret_cast<float*>(w + p.part_off);
   int before = 0;
   for (int i = 0; i < 3; ++i) {
     g.prob[i].kind = i;
     g.prob[i].M = Ms[i];
     g.prob[i].mtiles = (Ms[i] + kBM - 1) / kBM;
     g.prob[i].out = outs[i];
+    g.prob[i].part = part;
+    part += size_t(p.splits) * Ms[i] * kRank;
     g.tiles_before[i] = before;
     before += g.prob[i].mtiles;
   }
