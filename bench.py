@@ -400,6 +400,29 @@ def run_reference(args, world, rank):
     return 0
 
 
+def profile_op(args) -> int:
+    """Runs one op of the path --steps times on --workload with no timing, for a
+    profiler to capture (e.g. ncu -k regex:topk16 ... bench.py --profile-op topk)."""
+    from draft_selection_gb300 import build
+    build.build()
+    import draft_selection_gb300 as dfl2
+    torch.cuda.set_device(0)
+    case = Case(wl.WORKLOADS[args.workload], 1.0, torch.device("cuda", 0))
+    if args.profile_op in ("select", "walk"):
+        case.topk()
+    if args.profile_op == "walk":
+        case.select()
+    fn = {"topk": case.topk, "select": case.select, "walk": case.walk,
+          "conv": lambda: case.conv(0), "tail": case.tail, "step": case.step}[args.profile_op]
+    for _ in range(args.steps):
+        fn()
+    torch.cuda.synchronize()
+    err = dfl2.dfl2_device_error()
+    print(json.dumps({"profile_op": args.profile_op, "workload": args.workload,
+                      "calls": args.steps, "device_error": err}), flush=True)
+    return 0 if err == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,7 +433,11 @@ def main():
     ap.add_argument("--batched", default=BATCHED, help="second workload ('' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--profile-op", choices=["topk", "select", "walk", "conv", "tail", "step"],
+                    help="run one op --steps times, untimed, for a profiler; no JSON line")
     args = ap.parse_args()
+    if args.profile_op:
+        return profile_op(args)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

@@ -29,16 +29,16 @@ namespace dfl2 {
 namespace {
 
 constexpr int kCBM = 128, kCBK = 64, kCThreads = 256;
-constexpr int kCMaxStages = 4;
+constexpr int kCMaxStages = 8;
 constexpr int kCMaxNG = 64;          // groups per CTA: N = 2*NG <= 128
 constexpr int kCMaxSplits = 8;       // portable cluster size
 constexpr int kCAStage = kCBM * kCBK * 2;  // 16 KB
+constexpr size_t kCSmemMax = 227 * 1024;
 
 struct ConvArgs {
-  const __nv_bfloat16* x;       // [R, d]
+  const __nv_bfloat16* x;       // [R, d] (the mix; the GEMM reads x through tmX)
   const __nv_bfloat16* x_prev;  // [B, d]
   const float* base;            // [2, d]
-  const __nv_bfloat16* W_c;     // [2G, d]
   __nv_bfloat16* y;             // [R, d]
   int R, L, d, G;
   int NG, ntiles, splits, kps, kblocks, stages;
@@ -47,36 +47,42 @@ struct ConvArgs {
 
 __host__ __device__ constexpr int conv_bstage_bytes(int NG) { return 2 * NG * kCBK * 2; }
 __host__ __device__ constexpr int conv_pitch(int NG) { return 2 * NG + 4; }  // fp32 per row
-
-// Operand stages: as many as fit beside the other regions (more in flight at batch 1).
-__host__ __device__ constexpr int conv_stages(int) { return 4; }
-__host__ __device__ size_t conv_tile_bytes(int NG) { return size_t(kCBM) * conv_pitch(NG) * 4; }
-__host__ __device__ size_t conv_stage_area(int NG) {
-  return size_t(conv_stages(NG)) * (kCAStage + conv_bstage_bytes(NG));
+__host__ __device__ constexpr size_t conv_tile_bytes(int NG) {
+  return size_t(kCBM) * conv_pitch(NG) * 4;
+}
+// The corrections tile reuses the operand stages once the mainloop is over.
+__host__ __device__ constexpr size_t conv_stage_area(int NG, int stages) {
+  return size_t(stages) * (kCAStage + conv_bstage_bytes(NG)) > conv_tile_bytes(NG)
+             ? size_t(stages) * (kCAStage + conv_bstage_bytes(NG))
+             : conv_tile_bytes(NG);
 }
 // Receive slots for split K: S slots of ceil(128/S) rows, at most 128 + S rows.
-// K is only split when the narrowest group slice (16) leaves the GPU short of tiles.
-__host__ __device__ size_t conv_recv_bytes(int NG) {
-  return NG == 16 ? size_t(kCBM + kCMaxSplits) * conv_pitch(NG) * 4 : 0;
+__host__ __device__ constexpr size_t conv_recv_bytes(int NG, int splits) {
+  return splits > 1 ? size_t(kCBM + kCMaxSplits) * conv_pitch(NG) * 4 : 0;
 }
-size_t conv_smem_bytes(int NG) {
-  // [operand stages] [corrections] [receive slots] [base slice] [barriers]
-  return 1024 + conv_stage_area(NG) + conv_tile_bytes(NG) + conv_recv_bytes(NG) +
+__host__ __device__ constexpr size_t conv_smem_bytes(int NG, int stages, int splits) {
+  // [operand stages | corrections] [receive slots] [base slice] [barriers]
+  return 1024 + conv_stage_area(NG, stages) + conv_recv_bytes(NG, splits) +
          size_t(2) * 16 * NG * 4 + 256;
 }
 
-__global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constant__ ConvArgs a) {
+// Warp roles: 0 = TMA producer (one thread), 1 = TMEM owner and MMA issuer (one
+// thread), 2-3 = the base slice, 4-7 = TMEM -> corrections; then all 8 mix.
+__global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constant__ ConvArgs a,
+                                                            const __grid_constant__ CUtensorMap tmX,
+                                                            const __grid_constant__ CUtensorMap tmW) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const int NG = a.NG, N = 2 * NG, pitch = conv_pitch(NG);
   const int bst = conv_bstage_bytes(NG);
-  const int kCStages = a.stages;
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + size_t(kCStages) * kCAStage;
-  float* corr = reinterpret_cast<float*>(smem + conv_stage_area(NG));  // [128][pitch]
-  float* recv = corr + size_t(kCBM) * pitch;                             // [S][rows_per][pitch]
-  float* bslice = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(recv) + conv_recv_bytes(NG));
+  const int nst = a.stages;
+  uint8_t* sA = smem;                                   // [stages][128 rows][128 B]
+  uint8_t* sB = smem + size_t(nst) * kCAStage;          // [stages][2*NG rows][128 B]
+  float* corr = reinterpret_cast<float*>(smem);         // [128][pitch], after the mainloop
+  float* recv = reinterpret_cast<float*>(smem + conv_stage_area(NG, nst));  // [S][rows_per][pitch]
+  float* bslice = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(recv) +
+                                           conv_recv_bytes(NG, a.splits));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * NG);
   uint64_t* empty_bar = full_bar + kCMaxStages;
   uint64_t* accum_bar = empty_bar + kCMaxStages;
@@ -92,72 +98,45 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   const uint32_t ncols = N < 32 ? 32u : static_cast<uint32_t>(N);
 
   if (tid == 0) {
-    for (int s = 0; s < kCStages; ++s) {
-      mbar_init(&full_bar[s], 4 * 32);  // the 128 producer threads
+    for (int s = 0; s < nst; ++s) {
+      mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     mbar_init(accum_bar, 1);
     fence_mbar_init();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
   }
-  if (warp == 4) tmem_alloc(tmem_slot, ncols);
+  if (warp == 1) tmem_alloc(tmem_slot, ncols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   pdl_wait();
-  if (warp >= 5) {  // idle during the mainloop: the base slice for the CTA's channels
-    for (int e = tid - 5 * 32; e < 2 * 16 * NG; e += kCThreads - 5 * 32) {
-      const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
-      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
-    }
-  }
 
-  if (warp < 4) {
-    // ---- producers: 128 x rows and 2*NG W_c rows, 16-byte chunks, 128-byte swizzle ----
-    const int j = tid & 7;
-    const __nv_bfloat16* xs[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = m0 + (tid >> 3) + 16 * i;
-      xs[i] = r < a.R ? a.x + size_t(r) * a.d : nullptr;
-    }
-    for (int it = 0; it < nkb; ++it) {
-      const int s = it % kCStages;
-      if (it >= kCStages && !mbar_wait(&empty_bar[s], ((it / kCStages) - 1) & 1))
-        record_error(a.err, kDevErrConv);
-      const int kc = (kb0 + it) * kCBK + j * 8;  // first column of this thread's chunk
-      const bool kok = kc < a.d;
-      uint8_t* dA = sA + size_t(s) * kCAStage;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int r = (tid >> 3) + 16 * i;
-        const bool ok = kok && xs[i] != nullptr;
-        cp_async16(dA + r * 128 + ((j ^ (r & 7)) << 4), ok ? xs[i] + kc : a.x, ok);
-      }
-      uint8_t* dB = sB + size_t(s) * bst;
-      for (int r = tid >> 3; r < N; r += 16) {
-        const int g = g0 + (r < NG ? r : r - NG);
-        const int wrow = (r < NG ? 0 : a.G) + g;
-        const bool ok = kok && g < a.G;
-        cp_async16(dB + r * 128 + ((j ^ (r & 7)) << 4),
-                   ok ? a.W_c + size_t(wrow) * a.d + kc : a.W_c, ok);
-      }
-      cp_async_commit();
-      if (it >= 2) {
-        cp_async_wait<2>();
-        fence_proxy_async_smem();
-        mbar_arrive(&full_bar[(it - 2) % kCStages]);
+  if (warp == 0) {
+    if (lane == 0) {  // ---- producer: x rows and both taps' W_c rows by TMA ----
+      const uint32_t tx = static_cast<uint32_t>(kCAStage + bst);
+      for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
+        if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrConv);
+        const int k0 = (kb0 + it) * kCBK;
+        mbar_arrive_expect_tx(&full_bar[s], tx);
+        tma_load_2d(sA + size_t(s) * kCAStage, &tmX, k0, m0, &full_bar[s]);
+        uint8_t* dB = sB + size_t(s) * bst;
+        tma_load_2d(dB, &tmW, k0, g0, &full_bar[s]);
+        tma_load_2d(dB + NG * 128, &tmW, k0, a.G + g0, &full_bar[s]);
+        if (++s == nst) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    for (int it = max(0, nkb - 2); it < nkb; ++it) mbar_arrive(&full_bar[it % kCStages]);
-  } else {
-    if (warp == 4 && lane == 0) {
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer ----
       const uint32_t idesc = umma_idesc_bf16(kCBM, N);
-      for (int it = 0; it < nkb; ++it) {
-        const int s = it % kCStages;
-        if (!mbar_wait(&full_bar[s], (it / kCStages) & 1)) record_error(a.err, kDevErrConv);
+      for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
+        if (!mbar_wait(&full_bar[s], ph)) record_error(a.err, kDevErrConv);
         tc_fence_after();
         const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kCAStage);
         const uint64_t bd = umma_desc_sw128(sB + size_t(s) * bst);
@@ -165,12 +144,23 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
         for (int k = 0; k < kCBK / 16; ++k)
           umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
         umma_commit(&empty_bar[s]);
+        if (++s == nst) {
+          s = 0;
+          ph ^= 1;
+        }
       }
       umma_commit(accum_bar);
     }
     __syncwarp();
+  } else if (warp < 4) {  // idle during the mainloop: the base slice for the CTA's channels
+    for (int e = tid - 64; e < 2 * 16 * NG; e += 64) {
+      const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
+      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+    }
+  } else {
     // ---- TMEM -> the corrections (one split), or push this split's partial rows
-    // into the receive slot of the CTA that owns them (split K) ----
+    // into the receive slot of the CTA that owns them (split K).  The accumulator
+    // is complete only when every MMA, and so every read of the stages, is done. ----
     const int quarter = warp & 3;
     if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
     tc_fence_after();
@@ -220,7 +210,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
     }
     __syncthreads();
   }
-  if (warp == 4) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
@@ -502,7 +492,7 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   if (e != cudaSuccess) return e;
   if (!g_conv_attr[dev & 63]) {
     e = cudaFuncSetAttribute(conv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(std::max(conv_smem_bytes(16), conv_smem_bytes(kCMaxNG))));
+                             static_cast<int>(kCSmemMax));
     if (e != cudaSuccess) return e;
     g_conv_attr[dev & 63] = true;
   }
@@ -547,7 +537,6 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   a.x = x;
   a.x_prev = x_prev;
   a.base = base;
-  a.W_c = W_c;
   a.y = y;
   a.R = B * L;
   a.L = L;
@@ -568,10 +557,21 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   want = std::min(want, a.kblocks);
   a.kps = (a.kblocks + want - 1) / want;
   a.splits = (a.kblocks + a.kps - 1) / a.kps;  // every split gets at least one K block
-  a.stages = conv_stages(NG);
   if (a.splits > 1 && NG != 16) return cudaErrorInvalidConfiguration;  // receive slots need NG 16
+  // As many operand stages as the shared memory of one CTA per SM holds, or of
+  // two when the tiles outnumber the SMs; never more than the K blocks.
+  const size_t budget = (long long)tiles * a.splits > sms ? size_t(112) * 1024 : kCSmemMax;
+  const size_t fixed = conv_smem_bytes(NG, 0, a.splits) - conv_stage_area(NG, 0);
+  const size_t per_stage = size_t(kCAStage) + conv_bstage_bytes(NG);
+  int stages = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 2;
+  stages = std::max(2, std::min({stages, kCMaxStages, std::max(a.kps, 2)}));
+  a.stages = stages;
+  alignas(64) CUtensorMap tmX, tmW;
+  if (!tensor_map_bf16(x, uint64_t(a.R), uint64_t(d), kCBM, &tmX) ||
+      !tensor_map_bf16(W_c, uint64_t(2) * a.G, uint64_t(d), static_cast<uint32_t>(NG), &tmW))
+    return cudaErrorInvalidValue;
   return launch_kc(conv_tc_kernel, dim3(tiles * a.splits), dim3(kCThreads),
-                   conv_smem_bytes(NG), s, true, a.splits, a);
+                   conv_smem_bytes(NG, stages, a.splits), s, true, a.splits, a, tmX, tmW);
 }
 
 }  // namespace dfl2

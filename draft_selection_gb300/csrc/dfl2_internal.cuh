@@ -83,6 +83,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- a counter one thread publishes to the rest of its CTA -----------------
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Bounded wait until *p > n; false on timeout.
+__device__ __forceinline__ bool wait_count_above(const uint32_t* p, uint32_t n) {
+  if (ld_acquire_cta(p) > n) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_cta(p) <= n) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
 // ---- named barrier for a subset of warps ---------------------------------
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -518,7 +518,8 @@ struct TmapEntry {
   CUtensorMap map;
 };
 std::mutex g_tmap_mu;
-TmapEntry g_tmap_cache[32];
+constexpr int kTmapCache = 128;
+TmapEntry g_tmap_cache[kTmapCache];
 int g_tmap_n = 0, g_tmap_next = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 }  // namespace
@@ -556,8 +557,8 @@ bool tensor_map_bf16(const void* base, uint64_t rows, uint64_t cols, uint32_t bo
     return false;
   TmapEntry& t = g_tmap_cache[g_tmap_next];
   t = TmapEntry{dev, base, rows, cols, box_rows, m};
-  g_tmap_next = (g_tmap_next + 1) % 32;
-  g_tmap_n = std::min(g_tmap_n + 1, 32);
+  g_tmap_next = (g_tmap_next + 1) % kTmapCache;
+  g_tmap_n = std::min(g_tmap_n + 1, kTmapCache);
   memcpy(out128, &m, sizeof(CUtensorMap));
   return true;
 }

@@ -10,9 +10,12 @@
 //     bulk async copies (cp.async.bulk, completion on mbarriers); eight
 //     consumer warps read the tiles from shared memory, two 16-byte vectors
 //     per lane per tile (each warp: two blocks of 32 vectors).
-//   * Bound: the first tiles of each row segment are held while every warp
-//     reduces its block maxima; the 16th largest of those maxima (16 distinct
-//     elements, so no larger than the row's 16th value) becomes the bound T.
+//   * Bound: the first tiles of each row segment are held while every lane
+//     takes the maximum of its own elements in them; the 16th largest of those
+//     lane maxima (maxima of 16 disjoint element sets, so no larger than the
+//     segment's 16th value) becomes the bound T.  Each warp sorts its 32 lane
+//     maxima and the 16th largest of the union is found by rank with binary
+//     searches over the other warps' sorted lists.
 //   * Candidates: every element >= T is appended, as a 64-bit key
 //     (ordered value << 32 | ~index, unique, larger = better), to a shared
 //     candidate buffer with one warp-aggregated atomic; a tile with no such
@@ -34,24 +37,22 @@ namespace {
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = 8192;
-constexpr int kStages = 7;
+constexpr int kVecPerLane = kTileBytes / 16 / 32;  // 16-byte vectors per lane per tile
+constexpr int kStages = 12;
 constexpr int kMaxGrid = 2048;
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kBlocksPerTile = 2 * kConsumerWarps;  // blocks of 32 vectors (512 bytes)
-// Tiles at the start of each row segment that feed the block-maximum bound;
-// later tiles skip the reduction and the CTA barrier.
-constexpr int kBoundTiles = 3;
 constexpr int kCandCap = 1024;   // candidate keys buffered per row segment
+constexpr int kRaise = 64;       // candidates per bound-raising window (2 per lane)
 constexpr int kMinTilesPerCta = 4;
-static_assert(kBoundTiles < kStages, "held bound tiles must leave the ring room to stream");
 constexpr int kConsumers = kConsumerWarps * 32;
-// [stages][full][empty][cand][extra: per-warp overflow lists][res][block maxima][flags]
+// [stages][full][empty][cand][extra: per-warp overflow lists][res][lane maxima][flags]
 constexpr size_t kSmemBytes = size_t(kStages) * kTileBytes + 2 * kStages * sizeof(uint64_t) +
                               size_t(kCandCap) * sizeof(uint64_t) +
                               size_t(kConsumerWarps) * kCand * sizeof(uint64_t) +
                               kCand * sizeof(uint64_t) +
-                              size_t(kBoundTiles) * kBlocksPerTile * sizeof(float) + 32;
-static_assert(kTileBytes == kBlocksPerTile * 32 * 16, "a tile is one iteration of all warps");
+                              size_t(kConsumerWarps) * kCand * sizeof(float) + 32;  // flags: 5 words
+static_assert(kVecPerLane <= 32, "hit masks are 32 bits");
+static_assert(kStages >= kConsumerWarps, "the held bound tiles must fit in the ring");
 
 struct TopkArgs {
   const uint8_t* logits;
@@ -86,6 +87,20 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t x, int lane) {
       const uint64_t y = shfl_xor64(x, j);
       const bool keep_max = (((lane & j) == 0) == ((lane & k) == 0));
       x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+    }
+  }
+  return x;
+}
+
+// Bitonic sort of one float per lane, descending across lanes 0..31.
+__device__ __forceinline__ float warp_sort32_desc_f(float x, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float y = __shfl_xor_sync(kFull, x, j);
+      const bool keep_max = (((lane & j) == 0) == ((lane & k) == 0));
+      x = keep_max ? fmaxf(x, y) : fminf(x, y);
     }
   }
   return x;
@@ -143,12 +158,6 @@ __device__ __forceinline__ void unpack(const uint4& q, float (&f)[EPV]) {
   }
 }
 
-__device__ __forceinline__ float warp_max_f(float x) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
-  return x;
-}
-
 // Maximum of one 16-byte vector, as float.
 template <int EPV>
 __device__ __forceinline__ float vec_max(const uint4& q) {
@@ -187,45 +196,49 @@ __device__ __forceinline__ void insert_lane_keys(WarpTop& w, uint64_t cand, int 
   }
 }
 
-// The lane's elements at or above the bound go to the CTA candidate buffer
-// (or, past its capacity, into the warp's own exact list).
+// The lane's elements of one 16-byte vector at or above the bound go to the
+// CTA candidate buffer with one warp-aggregated atomic (or, past its
+// capacity, into the warp's own exact list).
 template <int EPV>
-__device__ __forceinline__ void collect_hits(WarpTop& w, const uint4& qa, const uint4& qb, bool va,
-                                             bool vb, uint32_t idxA, uint32_t idxB, int lane,
-                                             uint64_t* cand, uint32_t* cand_count) {
-  float f[2 * EPV];
-  {
-    float fa[EPV], fb[EPV];
-    unpack<EPV>(qa, fa);
-    unpack<EPV>(qb, fb);
-#pragma unroll
-    for (int e = 0; e < EPV; ++e) {
-      f[e] = fa[e];
-      f[EPV + e] = fb[e];
-    }
-  }
+__device__ __forceinline__ void collect_vec(WarpTop& w, const uint4& q, bool valid, uint32_t idx0,
+                                            int lane, uint64_t* cand, uint32_t* cand_count,
+                                            uint32_t* raise_s) {
+  float f[EPV];
+  unpack<EPV>(q, f);
   uint32_t mask = 0;
 #pragma unroll
-  for (int e = 0; e < 2 * EPV; ++e)
-    if ((e < EPV ? va : vb) && f[e] >= w.bound) mask |= 1u << e;
+  for (int e = 0; e < EPV; ++e)
+    if (valid && f[e] >= w.bound) mask |= 1u << e;
   const int n = __popc(mask);
-  int pre = n;  // inclusive warp scan of the counts
+  const unsigned who = __ballot_sync(kFull, n != 0);
+  if (!who) return;
+  int pre, total;
+  uint32_t base;
+  if ((who & (who - 1)) == 0) {  // one lane hits (the common case): no scan
+    const int src = __ffs(who) - 1;
+    total = __shfl_sync(kFull, n, src);
+    pre = n;
+    uint32_t b0 = 0;
+    if (lane == src) b0 = atomicAdd(cand_count, static_cast<uint32_t>(n));
+    base = __shfl_sync(kFull, b0, src);
+  } else {
+    pre = n;  // inclusive warp scan of the counts
 #pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int o = __shfl_up_sync(kFull, pre, off);
-    if (lane >= off) pre += o;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFull, pre, off);
+      if (lane >= off) pre += o;
+    }
+    total = __shfl_sync(kFull, pre, 31);
+    uint32_t b0 = 0;
+    if (lane == 0) b0 = atomicAdd(cand_count, static_cast<uint32_t>(total));
+    base = __shfl_sync(kFull, b0, 0);
   }
-  const int total = __shfl_sync(kFull, pre, 31);
-  uint32_t base = 0;
-  if (lane == 0) base = atomicAdd(cand_count, static_cast<uint32_t>(total));
-  base = __shfl_sync(kFull, base, 0);
   uint32_t pos = base + static_cast<uint32_t>(pre - n);
   uint32_t over = 0;  // elements that did not fit
 #pragma unroll
-  for (int e = 0; e < 2 * EPV; ++e) {
+  for (int e = 0; e < EPV; ++e) {
     if ((mask >> e) & 1u) {
-      const uint64_t k = make_key(f[e], e < EPV ? idxA + e : idxB + (e - EPV));
-      if (pos < kCandCap) cand[pos] = k;
+      if (pos < kCandCap) cand[pos] = make_key(f[e], idx0 + e);
       else over |= 1u << e;
       ++pos;
     }
@@ -237,11 +250,69 @@ __device__ __forceinline__ void collect_hits(WarpTop& w, const uint4& qa, const 
       over &= over - 1;
       float v = f[0];
 #pragma unroll
-      for (int e2 = 1; e2 < 2 * EPV; ++e2) v = (e2 == e) ? f[e2] : v;
-      k = make_key(v, e < EPV ? idxA + e : idxB + (e - EPV));
+      for (int e2 = 1; e2 < EPV; ++e2) v = (e2 == e) ? f[e2] : v;
+      k = make_key(v, idx0 + e);
     }
     insert_lane_keys(w, k, lane);
   }
+  // Raising the bound: the warp whose keys complete a window of kRaise buffer
+  // slots ranks that window (two slots per lane, the lane's larger one).  The
+  // 16th largest of those 32 maxima stands for 16 distinct elements of the
+  // segment, so it is still a lower bound on the segment's 16th value.  Slots
+  // other warps have reserved but not yet written read as empty (the buffer is
+  // cleared at every segment's end), which only lowers the result.
+  const uint32_t end = base + static_cast<uint32_t>(total);
+  if (end / kRaise != base / kRaise && end <= static_cast<uint32_t>(kCandCap)) {
+    __syncwarp();
+    const uint32_t m0 = (end / kRaise - 1) * kRaise;
+    const volatile uint64_t* wnd = cand + m0;
+    const uint64_t k0 = wnd[2 * lane], k1 = wnd[2 * lane + 1];
+    float v = -INFINITY;
+    if (k0 != 0ull) v = unord_f32(static_cast<uint32_t>(k0 >> 32));
+    if (k1 != 0ull) v = fmaxf(v, unord_f32(static_cast<uint32_t>(k1 >> 32)));
+    v = warp_sort32_desc_f(v, lane);
+    const float nb = __shfl_sync(kFull, v, kCand - 1);
+    if (nb > w.bound) {
+      w.bound = nb;
+      if (lane == 0) atomicMax(raise_s, ord_f32(nb));
+    }
+  }
+}
+
+// One warp's pass over one staged tile: the lane reads vectors lane + 32*j,
+// j < 16; vectors whose maximum reaches the bound are re-read and collected.
+template <int EPV>
+__device__ __forceinline__ void scan_tile(WarpTop& w, const uint4* tile, int nvec, uint32_t elem_base,
+                                          int lane, uint64_t* cand, uint32_t* cand_count,
+                                          uint32_t* raise_s) {
+  uint32_t hit = 0;
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j) {
+    const int v = lane + 32 * j;
+    if (v < nvec && vec_max<EPV>(tile[v]) >= w.bound) hit |= 1u << j;
+  }
+  uint32_t any = __reduce_or_sync(kFull, hit);
+  while (any) {
+    const int j = __ffs(any) - 1;
+    any &= any - 1;
+    const int v = lane + 32 * j;
+    const bool ok = v < nvec;
+    const uint4 q = ok ? tile[v] : make_uint4(0u, 0u, 0u, 0u);
+    collect_vec<EPV>(w, q, ok, elem_base + static_cast<uint32_t>(v) * EPV, lane, cand, cand_count,
+                     raise_s);
+  }
+}
+
+// The lane's maximum over its vectors of a staged tile.
+template <int EPV>
+__device__ __forceinline__ float lane_max_tile(const uint4* tile, int nvec, int lane) {
+  float m = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j) {
+    const int v = lane + 32 * j;
+    if (v < nvec) m = fmaxf(m, vec_max<EPV>(tile[v]));
+  }
+  return m;
 }
 
 __device__ __forceinline__ void write_row(const TopkArgs& a, long long row, uint64_t key, int lane) {
@@ -270,18 +341,33 @@ __device__ __forceinline__ void rank_select16(const uint64_t* keys, int n, uint6
   }
 }
 
-// The 16th largest of n block maxima (ties ranked by position); -inf if n < 16.
-__device__ __forceinline__ void rank_bound(const float* bm, int n, float* out, int tid) {
-  for (int i = tid; i < n; i += kConsumers) {
-    const float v = bm[i];
-    int r = 0;
-    for (int j = 0; j < n; ++j) r += (bm[j] > v) || (bm[j] == v && j < i);
-    if (r == kCand - 1) *out = v;
+// lm holds kConsumerWarps descending lists of 16 lane maxima.  Entry (w, i)
+// ranks as i plus, in every other list w2, the entries above it (ties go to
+// the lower list); the entry of rank 15 is the 16th largest of the union.
+__device__ __forceinline__ void rank_bound(const float* lm, float* out, int tid) {
+  if (tid >= kConsumerWarps * kCand) return;
+  const int w = tid / kCand;
+  const float v = lm[tid];
+  int r = tid % kCand;
+#pragma unroll
+  for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+    if (w2 == w) continue;
+    const float* L2 = lm + w2 * kCand;
+    int c = 0;
+#pragma unroll
+    for (int st = 16; st > 0; st >>= 1) {
+      if (c + st <= kCand) {
+        const float e = L2[c + st - 1];
+        if (e > v || (e == v && w2 < w)) c += st;
+      }
+    }
+    r += c;
   }
+  if (r == kCand - 1) *out = v;
 }
 
 template <int EPV>
-__global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) topk16_kernel(TopkArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kTileBytes);
@@ -289,10 +375,12 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
   uint64_t* cand = empty_bar + kStages;                          // [kCandCap]
   uint64_t* extra = cand + kCandCap;                              // [kConsumerWarps][16]
   uint64_t* res = extra + kConsumerWarps * kCand;                 // [16]
-  float* bmax = reinterpret_cast<float*>(res + kCand);            // [kBoundTiles][16]
-  uint32_t* last_flag = reinterpret_cast<uint32_t*>(bmax + kBoundTiles * kBlocksPerTile);
+  float* lmax = reinterpret_cast<float*>(res + kCand);            // [kConsumerWarps][16]
+  uint32_t* last_flag = reinterpret_cast<uint32_t*>(lmax + kConsumerWarps * kCand);
   uint32_t* cand_count = last_flag + 1;
   float* bound_s = reinterpret_cast<float*>(cand_count + 1);
+  uint32_t* raise_s = reinterpret_cast<uint32_t*>(bound_s + 1);  // raised bound, ordered bits
+  uint32_t* issued = raise_s + 1;  // tiles the producer has issued so far
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long T = a.total_tiles;
@@ -304,110 +392,106 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full_bar[s], 1);
-      mbar_init(&empty_bar[s], kConsumerWarps);
+      mbar_init(&empty_bar[s], 1);  // the one warp that scans the tile
     }
     fence_mbar_init();
     *cand_count = 0u;
+    *issued = 0u;
     for (int k = 0; k < kCand; ++k) res[k] = 0ull;
   }
+  for (int e = threadIdx.x; e < kCandCap; e += kThreads) cand[e] = 0ull;
   __syncthreads();
   pdl_wait();  // the logits may come from the previous kernel on the stream
 
   if (warp == kConsumerWarps) {  // producer
     if (lane == 0) {
-      for (long long g = g0; g < g1; ++g) {
-        const int i = static_cast<int>(g - g0), s = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty_bar[s], ((i / kStages) - 1) & 1))
-          record_error(a.err, kDevErrTopkEmpty);
-        const long long row = g / tpr;
-        const size_t off = size_t(g % tpr) * kTileBytes;
+      long long row = g0 / tpr;
+      int t = static_cast<int>(g0 - row * tpr);
+      const int n = static_cast<int>(g1 - g0);
+      for (int i = 0, s = 0, ph = 0; i < n; ++i) {
+        if (i >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrTopkEmpty);
+        const size_t off = size_t(t) * kTileBytes;
         const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
         mbar_arrive_expect_tx(&full_bar[s], bytes);
         bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + size_t(row) * row_bytes + off, bytes,
                  &full_bar[s]);
+        st_release_cta(issued, static_cast<uint32_t>(i + 1));
+        if (++t == tpr) {
+          t = 0;
+          ++row;
+        }
+        if (++s == kStages) {
+          s = 0;
+          ph ^= 1;
+        }
       }
     }
     return;
   }
 
+  // Tile i of this CTA (0-based over its share) sits in stage i % kStages and
+  // is scanned by warp i % kConsumerWarps.  Warps do not move in step, so a
+  // warp may reach tile i while the producer still waits to reuse the stage
+  // for tile i - kStages: the stage's full barrier is then two phases behind
+  // and its parity alone cannot tell.  A warp therefore first waits until the
+  // producer has issued tile i (which it does only after tile i - kStages was
+  // released), and only then on the barrier's parity.
   long long g = g0;
-  int i = 0, seg = 0;
+  long long row = g0 / tpr;
+  int t0 = static_cast<int>(g0 - row * tpr);  // tile of the row where the segment starts
+  int i0 = 0;                                  // CTA tile index where the segment starts
   while (g < g1) {
-    const long long row = g / tpr;
     const long long seg_end = min(g1, (row + 1) * tpr);
+    const int nseg = static_cast<int>(seg_end - g);
+    const int nbound = nseg < kConsumerWarps ? nseg : kConsumerWarps;
     WarpTop w{0ull, -INFINITY};
-    const int nbound = static_cast<int>((seg_end - g < kBoundTiles ? seg_end - g : kBoundTiles));
-    // ---- bound: hold the first nbound tiles, rank their block maxima ----
-    uint4 hqa[kBoundTiles], hqb[kBoundTiles];
-    bool hva[kBoundTiles], hvb[kBoundTiles];
-    float hma[kBoundTiles], hmb[kBoundTiles];
-    uint32_t hia[kBoundTiles], hib[kBoundTiles];
-#pragma unroll
-    for (int k = 0; k < kBoundTiles; ++k) {
-      hva[k] = hvb[k] = false;
-      hma[k] = hmb[k] = -INFINITY;
-      hqa[k] = hqb[k] = make_uint4(0u, 0u, 0u, 0u);
-      hia[k] = hib[k] = 0u;
-      if (k < nbound) {
-        const int s = (i + k) % kStages;
-        if (!mbar_wait(&full_bar[s], ((i + k) / kStages) & 1)) record_error(a.err, kDevErrTopkFull);
-        const int t = static_cast<int>((g + k) % tpr);
-        const int nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
-        const uint32_t elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
-        const uint4* tile = reinterpret_cast<const uint4*>(stages + size_t(s) * kTileBytes);
-        const int v_a = warp * 64 + lane, v_b = v_a + 32;
-        hva[k] = v_a < nvec;
-        hvb[k] = v_b < nvec;
-        if (hva[k]) hqa[k] = tile[v_a];
-        if (hvb[k]) hqb[k] = tile[v_b];
-        hma[k] = hva[k] ? vec_max<EPV>(hqa[k]) : -INFINITY;
-        hmb[k] = hvb[k] ? vec_max<EPV>(hqb[k]) : -INFINITY;
-        hia[k] = elem_base + static_cast<uint32_t>(v_a) * EPV;
-        hib[k] = elem_base + static_cast<uint32_t>(v_b) * EPV;
-        const float bma = warp_max_f(hma[k]), bmb = warp_max_f(hmb[k]);
-        if (lane == 0) {
-          bmax[k * kBlocksPerTile + 2 * warp] = bma;
-          bmax[k * kBlocksPerTile + 2 * warp + 1] = bmb;
-        }
+    // this warp's first tile of the segment (segment-relative)
+    const int jw = ((warp - i0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
+    auto tile_of = [&](int j, const uint4*& tile, int& nvec, uint32_t& elem_base) {
+      const int i = i0 + j, st = i % kStages;
+      if (!wait_count_above(issued, static_cast<uint32_t>(i)) ||
+          !mbar_wait(&full_bar[st], (i / kStages) & 1))
+        record_error(a.err, kDevErrTopkFull);
+      const int t = t0 + j;
+      nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
+      elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
+      tile = reinterpret_cast<const uint4*>(stages + size_t(st) * kTileBytes);
+    };
+    auto release = [&](int j) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[(i0 + j) % kStages]);
+    };
+    // ---- bound: the first nbound tiles (one per warp) stay staged while every
+    // lane takes its maximum over them; the 16th largest lane maximum is T ----
+    {
+      float lm = -INFINITY;
+      if (jw < nbound) {
+        const uint4* tile;
+        int nvec;
+        uint32_t eb;
+        tile_of(jw, tile, nvec, eb);
+        lm = lane_max_tile<EPV>(tile, nvec, lane);
       }
+      lm = warp_sort32_desc_f(lm, lane);
+      if (lane < kCand) lmax[warp * kCand + lane] = lm;
     }
-    if (threadIdx.x == 0) *bound_s = -INFINITY;  // read last at the previous segment's start
+    if (threadIdx.x == 0) {  // both read last at the previous segment's start
+      *bound_s = -INFINITY;
+      *raise_s = ord_f32(-INFINITY);
+    }
     named_sync(1, kConsumers);
-    rank_bound(bmax, nbound * kBlocksPerTile, bound_s, threadIdx.x);
+    rank_bound(lmax, bound_s, threadIdx.x);
     named_sync(1, kConsumers);
     w.bound = *bound_s;
-#pragma unroll
-    for (int k = 0; k < kBoundTiles; ++k) {
-      if (k < nbound) {
-        if (__any_sync(kFull, (hva[k] && hma[k] >= w.bound) || (hvb[k] && hmb[k] >= w.bound)))
-          collect_hits<EPV>(w, hqa[k], hqb[k], hva[k], hvb[k], hia[k], hib[k], lane, cand,
-                            cand_count);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[(i + k) % kStages]);
-      }
-    }
-    g += nbound;
-    i += nbound;
-    // ---- stream the rest of the segment against the bound ----
-    for (; g < seg_end; ++g, ++i) {
-      const int s = i % kStages;
-      if (!mbar_wait(&full_bar[s], (i / kStages) & 1)) record_error(a.err, kDevErrTopkFull);
-      const int t = static_cast<int>(g % tpr);
-      const size_t off = size_t(t) * kTileBytes;
-      const int nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - off) / 16);
-      const uint32_t elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
-      const uint4* tile = reinterpret_cast<const uint4*>(stages + size_t(s) * kTileBytes);
-      const int v_a = warp * 64 + lane, v_b = v_a + 32;
-      const bool ok_a = v_a < nvec, ok_b = v_b < nvec;
-      const uint4 qa = ok_a ? tile[v_a] : make_uint4(0u, 0u, 0u, 0u);
-      const uint4 qb = ok_b ? tile[v_b] : make_uint4(0u, 0u, 0u, 0u);
-      const float ma = ok_a ? vec_max<EPV>(qa) : -INFINITY;
-      const float mb = ok_b ? vec_max<EPV>(qb) : -INFINITY;
-      if (__any_sync(kFull, (ok_a && ma >= w.bound) || (ok_b && mb >= w.bound)))
-        collect_hits<EPV>(w, qa, qb, ok_a, ok_b, elem_base + static_cast<uint32_t>(v_a) * EPV,
-                          elem_base + static_cast<uint32_t>(v_b) * EPV, lane, cand, cand_count);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    // ---- every tile of the segment against the bound (the held one first) ----
+    for (int j = jw; j < nseg; j += kConsumerWarps) {
+      const uint4* tile;
+      int nvec;
+      uint32_t eb;
+      tile_of(j, tile, nvec, eb);
+      w.bound = fmaxf(w.bound, unord_f32(*reinterpret_cast<volatile uint32_t*>(raise_s)));
+      scan_tile<EPV>(w, tile, nvec, eb, lane, cand, cand_count, raise_s);
+      release(j);
     }
 
     // ---- the segment's top 16 by rank over the candidates (+ overflow lists) ----
@@ -446,7 +530,8 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
       }
     }
     named_sync(1, kConsumers);
-    if (*last_flag) {
+    const bool was_last = *last_flag != 0u;
+    if (was_last) {
       // Last CTA of a split row: rank the partial lists, kCandCap - 16 keys at a
       // time, carrying the running top 16 in front of each batch.
       __threadfence();
@@ -469,7 +554,16 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
       }
       named_sync(1, kConsumers);
     }
-    ++seg;
+    // Clear the slots this segment used: the next segment's bound raises read
+    // slots that are reserved but not yet written as empty.
+    {
+      const int used = was_last ? kCandCap : ncand;
+      for (int e = threadIdx.x; e < used; e += kConsumers) cand[e] = 0ull;
+    }
+    g = seg_end;
+    i0 += nseg;
+    ++row;
+    t0 = 0;
   }
   pdl_launch_dependents();
 }

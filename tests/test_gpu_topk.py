@@ -153,3 +153,19 @@ def test_degenerate_rows():
         idx, val = gpu_topk(x.cuda())
         check_rows(x, idx, val)
     assert idx[0, 0].tolist() == list(range(16))
+
+
+def test_adversarial_long_rows():
+    """Full-vocabulary rows whose order defeats an early bound: rising values (every
+    element beats everything before it, so the candidate buffer fills and the bound
+    keeps rising), falling values, one constant (all tied), a sawtooth with a rising
+    envelope, and rows with their winners spread one per tile."""
+    V = 151936
+    ar = torch.arange(V, dtype=torch.float32)
+    rows = [ar / 64.0, -ar / 64.0, torch.full((V,), 0.25),
+            (ar % 4096) / 4096.0 + ar / V,
+            torch.where(ar % 4096 == 17, 3.0 + ar / V, torch.zeros(V))]
+    for dt in (torch.float32, torch.bfloat16):
+        lg = torch.stack(rows).view(1, len(rows), V).to(dt)
+        idx, val = gpu_topk(lg.cuda())
+        check_rows(lg, idx, val)
