@@ -568,6 +568,352 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_kernel(TopkArgs a) {
   pdl_launch_dependents();
 }
 
+// ============================================================================
+// Few rows (batch 1 and small batches): one thread-block cluster per row.
+//
+// The persistent kernel above balances any number of rows, but at batch 1 its
+// per-segment bound, ranking and the global ticket merge of about ten partial
+// lists per row form a long dependent chain.  Here the C CTAs of a cluster
+// share one row (C <= 8), each streaming at most kRMaxTilesPerCta tiles, and
+// the chain is kept short: warp-collective sorting networks (tens of
+// dependent shuffles each) are replaced by counting that runs in parallel.
+//   * Each lane takes its maximum key (value, then lowest index) over its
+//     vectors of the warp's first tile; a lane learns its rank among the
+//     warp's 32 maxima from 32 independent shuffles, which lays out each
+//     warp's best 16 in order, and binary searches in the other warps' lists
+//     rank those 128.  The 16th largest, T, bounds the CTA's share of the row
+//     (16 distinct elements reach it).
+//   * Every element whose key reaches T is appended to a shared buffer (a few
+//     dozen; a key bound also caps all-tied rows); the CTA's top 16 follow by
+//     counting, for each candidate, the candidates above it.
+//   * The CTAs hand their 16 keys to the cluster's first CTA through
+//     distributed shared memory and arrive on its mbarrier; it ranks the C
+//     lists by binary search in each.  No global atomics or fences.
+// ============================================================================
+constexpr int kRStages = 8;
+constexpr int kRMaxCluster = 8;
+constexpr int kRMaxTilesPerCta = 16;
+constexpr int kRCandCap = 1024;
+// Shared memory: [stages][full][empty][list barrier, pad][cand][extra][res]
+// [cluster lists][lane maxima][their top 16][flags]; every region after the
+// barriers starts on a 16-byte boundary (the lists are read 16 bytes at a time).
+constexpr size_t kROffBars = size_t(kRStages) * kTileBytes;
+constexpr size_t kROffCand = kROffBars + (2 * kRStages + 2) * sizeof(uint64_t);
+constexpr size_t kROffExtra = kROffCand + size_t(kRCandCap) * sizeof(uint64_t);
+constexpr size_t kROffRes = kROffExtra + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
+constexpr size_t kROffClists = kROffRes + kCand * sizeof(uint64_t);
+constexpr size_t kROffWsorted = kROffClists + size_t(kRMaxCluster) * kCand * sizeof(uint64_t);
+constexpr size_t kROffTres = kROffWsorted + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
+constexpr size_t kROffFlags = kROffTres + kCand * sizeof(uint64_t);
+constexpr size_t kRSmemBytes = kROffFlags + 16;
+static_assert(kROffCand % 16 == 0 && kROffExtra % 16 == 0 && kROffRes % 16 == 0 &&
+                  kROffClists % 16 == 0 && kROffWsorted % 16 == 0 && kROffTres % 16 == 0,
+              "16-byte aligned regions");
+static_assert(kConsumerWarps <= kRMaxCluster, "lists ranked by rank_sorted_lists16");
+
+struct RowsArgs {
+  const uint8_t* logits;
+  int V, tiles_per_row, C;
+  int32_t* out_idx;
+  float* out_val;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void st_cluster_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// The lane's largest key over its vectors of a staged tile (0 if it has none);
+// vm receives the vectors' maximum values.
+template <int EPV>
+__device__ __forceinline__ uint64_t lane_max_key(const uint4* tile, int nvec, uint32_t elem_base,
+                                                 int lane, float (&vm)[kVecPerLane]) {
+  float lm = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j) {
+    const int v = lane + 32 * j;
+    vm[j] = v < nvec ? vec_max<EPV>(tile[v]) : -INFINITY;
+    lm = fmaxf(lm, vm[j]);
+  }
+  uint32_t at = 0;  // vectors holding the maximum
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j)
+    if (lane + 32 * j < nvec && vm[j] == lm) at |= 1u << j;
+  if (at == 0u) return 0ull;
+  const int v = lane + 32 * (__ffs(at) - 1);
+  float f[EPV];
+  unpack<EPV>(tile[v], f);
+  uint32_t em = 0;
+#pragma unroll
+  for (int e = 0; e < EPV; ++e)
+    if (f[e] == lm) em |= 1u << e;  // -0.0 == +0.0, as the keys treat them
+  return make_key(lm, elem_base + static_cast<uint32_t>(v) * EPV + (__ffs(em) - 1));
+}
+
+// The lane's keys >= T (other than `skip`) over the vectors in `hit`, in a
+// fixed order; calls f(key) for each.
+template <int EPV, typename F>
+__device__ __forceinline__ void for_keys_at_least(const uint4* tile, uint32_t hit, uint32_t elem_base,
+                                                  int lane, uint64_t T, float bval, uint64_t skip,
+                                                  F&& f) {
+  for (uint32_t h = hit; h; h &= h - 1) {
+    const int j = __ffs(h) - 1;
+    const int v = lane + 32 * j;
+    float x[EPV];
+    unpack<EPV>(tile[v], x);
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+      if (x[e] < bval) continue;
+      const uint64_t k = make_key(x[e], elem_base + static_cast<uint32_t>(v) * EPV + e);
+      if (k >= T && k != skip) f(k);
+    }
+  }
+}
+
+// Appends the lane's keys >= T (other than `skip`) to `cand` (capacity
+// kRCandCap - 16) with one atomic per lane; keys past the capacity go, one per
+// lane per round, into the warp's exact list.
+template <int EPV>
+__device__ __forceinline__ void append_tile_keys(WarpTop& w, const uint4* tile, int nvec,
+                                                 uint32_t elem_base, const float (&vm)[kVecPerLane],
+                                                 uint64_t T, float bval, uint64_t skip, int lane,
+                                                 uint64_t* cand, uint32_t* cand_count) {
+  constexpr uint32_t kCap = kRCandCap - kCand;
+  uint32_t hit = 0;
+#pragma unroll
+  for (int j = 0; j < kVecPerLane; ++j)
+    if (lane + 32 * j < nvec && vm[j] >= bval) hit |= 1u << j;
+  uint32_t c = 0;
+  uint64_t k1 = 0ull, k2 = 0ull;  // the first two, kept to spare a second pass
+  for_keys_at_least<EPV>(tile, hit, elem_base, lane, T, bval, skip, [&](uint64_t k) {
+    if (c == 0) k1 = k;
+    else if (c == 1) k2 = k;
+    ++c;
+  });
+  const uint32_t pos = c ? atomicAdd(cand_count, c) : 0u;
+  const uint32_t first_spill = pos + c > kCap ? (pos >= kCap ? 0u : kCap - pos) : c;
+  if (c <= 2) {
+    if (c > 0 && first_spill > 0) cand[pos] = k1;
+    if (c > 1 && first_spill > 1) cand[pos + 1] = k2;
+  } else {
+    uint32_t o = 0;
+    for_keys_at_least<EPV>(tile, hit, elem_base, lane, T, bval, skip, [&](uint64_t k) {
+      if (o < first_spill) cand[pos + o] = k;
+      ++o;
+    });
+  }
+  // Rare: the buffer is full.  Each lane offers its spilled keys, largest
+  // first, one per round.
+  bool spill = first_spill < c;
+  uint64_t last = ~0ull;
+  while (__any_sync(kFull, spill)) {
+    uint64_t best = 0ull;
+    if (spill) {
+      uint32_t o = 0;
+      for_keys_at_least<EPV>(tile, hit, elem_base, lane, T, bval, skip, [&](uint64_t k) {
+        if (o >= first_spill && k < last && k > best) best = k;
+        ++o;
+      });
+      if (best == 0ull) spill = false;
+    }
+    insert_lane_keys(w, best, lane);
+    last = best;
+  }
+}
+
+// res[r] for r < 16: the key of rank r among n lists of 16 keys (0 = empty,
+// skipped; keys unique); thread t < 16n places key t of list t/16, given its
+// rank inside its own list (lists are descending), by counting the keys above
+// it in the other lists: independent loads, no dependent search.
+__device__ __forceinline__ void rank_lists16(const uint64_t* lists, int n, uint64_t* res, int tid) {
+  if (tid >= n * kCand) return;
+  const uint64_t v = lists[tid];
+  if (v == 0ull) return;
+  const int own = tid / kCand;
+  int r = tid % kCand;
+  for (int l = 0; l < n; ++l) {
+    if (l == own) continue;
+    const ulonglong2* L = reinterpret_cast<const ulonglong2*>(lists + l * kCand);
+#pragma unroll
+    for (int q = 0; q < kCand / 2; ++q) {
+      const ulonglong2 p = L[q];
+      r += (p.x > v) + (p.y > v);
+    }
+  }
+  if (r < kCand) res[r] = v;
+}
+
+template <int EPV>
+__global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kROffBars);
+  uint64_t* empty_bar = full_bar + kRStages;
+  uint64_t* list_bar = empty_bar + kRStages;  // first CTA: the others' lists arrived
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kROffCand);       // [kRCandCap]
+  uint64_t* extra = reinterpret_cast<uint64_t*>(smem + kROffExtra);     // [kConsumerWarps][16]
+  uint64_t* res = reinterpret_cast<uint64_t*>(smem + kROffRes);         // [16]
+  uint64_t* clists = reinterpret_cast<uint64_t*>(smem + kROffClists);   // [kRMaxCluster][16]
+  uint64_t* wsorted = reinterpret_cast<uint64_t*>(smem + kROffWsorted); // [warps][16] lane maxima
+  uint64_t* tres = reinterpret_cast<uint64_t*>(smem + kROffTres);       // [16] their top 16
+  uint32_t* cand_count = reinterpret_cast<uint32_t*>(smem + kROffFlags);
+  uint32_t* issued = cand_count + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.C, rank = static_cast<int>(blockIdx.x) % C;
+  const long long row = blockIdx.x / C;
+  const int tpr = a.tiles_per_row;
+  const int t_lo = rank * tpr / C, t_hi = (rank + 1) * tpr / C;  // this CTA's tiles of the row
+  const int n = t_hi - t_lo;
+  const size_t row_bytes = size_t(a.V) * (16 / EPV);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kRStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(list_bar, C > 1 ? C - 1 : 1);
+    fence_mbar_init();
+    *issued = 0u;
+    *cand_count = 0u;
+  }
+  if (threadIdx.x < kCand) {
+    res[threadIdx.x] = 0ull;
+    tres[threadIdx.x] = 0ull;
+  }
+  if (threadIdx.x < kConsumerWarps * kCand) wsorted[threadIdx.x] = 0ull;
+  __syncthreads();
+  if (C > 1) cluster_arrive_release();  // the list barrier is initialised (waited before use)
+  pdl_wait();  // the logits may come from the previous kernel on the stream
+
+  if (warp == kConsumerWarps) {  // producer
+    if (lane == 0) {
+      for (int i = 0, s = 0, ph = 0; i < n; ++i) {
+        if (i >= kRStages && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrTopkEmpty);
+        const size_t off = size_t(t_lo + i) * kTileBytes;
+        const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
+        mbar_arrive_expect_tx(&full_bar[s], bytes);
+        bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + size_t(row) * row_bytes + off, bytes,
+                 &full_bar[s]);
+        st_release_cta(issued, static_cast<uint32_t>(i + 1));
+        if (++s == kRStages) {
+          s = 0;
+          ph ^= 1;
+        }
+      }
+    }
+    if (C > 1) cluster_wait_acquire();
+  } else {
+    // Warp w scans tiles w, w + 8, ...: each stage serves one warp only.
+    auto stage_of = [&](int i, const uint4*& tile, int& nvec, uint32_t& eb) {
+      const int st = i % kRStages;
+      if (!wait_count_above(issued, static_cast<uint32_t>(i)) ||
+          !mbar_wait(&full_bar[st], (i / kRStages) & 1))
+        record_error(a.err, kDevErrTopkFull);
+      const int t = t_lo + i;
+      nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
+      eb = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
+      tile = reinterpret_cast<const uint4*>(stages + size_t(st) * kTileBytes);
+    };
+    WarpTop w{0ull, -INFINITY};
+    float vm[kVecPerLane];
+    const uint4* tile = nullptr;
+    int nvec = 0;
+    uint32_t eb = 0;
+    // ---- the bound T: the 16th largest lane-maximum key over the CTA's first
+    // wave of tiles.  A lane's rank in its warp (32 shuffles) puts the warp's
+    // best 16 in order; the 128 are then ranked by binary search. ----
+    uint64_t lk = 0ull;
+    if (warp < n) {
+      stage_of(warp, tile, nvec, eb);
+      lk = lane_max_key<EPV>(tile, nvec, eb, lane, vm);
+    }
+    {
+      int r = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r += shfl64(lk, j) > lk;
+      if (r < kCand && lk != 0ull) wsorted[warp * kCand + r] = lk;
+    }
+    const int nw = n < kConsumerWarps ? n : kConsumerWarps;
+    named_sync(1, kConsumers);
+    rank_lists16(wsorted, nw, tres, threadIdx.x);
+    named_sync(1, kConsumers);
+    const uint64_t T = tres[kCand - 1];  // 0 (fewer than 16 keys): accept all
+    const float bval = T ? unord_f32(static_cast<uint32_t>(T >> 32)) : -INFINITY;
+    // ---- candidates.  With T set, the 16 lane maxima at or above it (tres)
+    // are in; a lane that holds one adds its other elements >= T (rare), and
+    // later tiles add every element >= T.  Without T every element goes in.
+    // Slots 0..15 hold tres, appended keys start at 16. ----
+    if (threadIdx.x < kCand) cand[threadIdx.x] = T ? tres[threadIdx.x] : 0ull;
+    for (int i = warp; i < n; i += kConsumerWarps) {
+      if (i != warp) {
+        stage_of(i, tile, nvec, eb);
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) {
+          const int v = lane + 32 * j;
+          vm[j] = v < nvec ? vec_max<EPV>(tile[v]) : -INFINITY;
+        }
+        append_tile_keys<EPV>(w, tile, nvec, eb, vm, T, bval, 0ull, lane, cand + kCand,
+                              cand_count);
+      } else if (T == 0ull) {
+        append_tile_keys<EPV>(w, tile, nvec, eb, vm, 0ull, -INFINITY, 0ull, lane, cand + kCand,
+                              cand_count);
+      } else {
+        // only a lane whose maximum reaches T can hold more; its maximum is in tres
+        const bool holds = lk >= T;
+        float vmh[kVecPerLane];
+#pragma unroll
+        for (int j = 0; j < kVecPerLane; ++j) vmh[j] = holds ? vm[j] : -INFINITY;
+        append_tile_keys<EPV>(w, tile, nvec, eb, vmh, T, bval, lk, lane, cand + kCand, cand_count);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[i % kRStages]);
+    }
+    if (lane < kCand) extra[warp * kCand + lane] = w.list;
+    named_sync(1, kConsumers);
+    const uint32_t cnt = *reinterpret_cast<volatile uint32_t*>(cand_count);
+    if (cnt == 0u && T != 0ull) {
+      if (threadIdx.x < kCand) res[threadIdx.x] = tres[threadIdx.x];  // already in rank order
+    } else {
+      // The overflow lists sit right after the buffer, so one ranking covers both.
+      rank_select16(cand, cnt > static_cast<uint32_t>(kRCandCap - kCand)
+                              ? kRCandCap + kConsumerWarps * kCand
+                              : kCand + static_cast<int>(cnt),
+                    res, threadIdx.x);
+    }
+    named_sync(1, kConsumers);
+    // ---- this CTA's 16 keys (descending: res[r] has rank r) to the first CTA ----
+    if (C == 1) {
+      if (threadIdx.x < kCand) clists[threadIdx.x] = res[threadIdx.x];
+    } else {
+      if (warp == 0) cluster_wait_acquire();
+      if (rank == 0) {
+        if (threadIdx.x < kCand) clists[threadIdx.x] = res[threadIdx.x];
+      } else if (threadIdx.x == 0) {
+#pragma unroll
+        for (int q = 0; q < kCand; ++q)
+          st_cluster_u64(dsmem_addr(clists + rank * kCand + q, 0u), res[q]);
+        mbar_arrive_remote(list_bar, 0u);  // release: the 16 stores above come first
+      }
+      if (warp != 0) cluster_wait_acquire();
+    }
+  }
+  if (rank == 0 && warp < kConsumerWarps) {
+    if (C > 1 && !mbar_wait_cluster(list_bar, 0)) record_error(a.err, kDevErrTopkFull);
+    named_sync(1, kConsumers);  // the first CTA's own list is in place too
+    if (threadIdx.x < kCand) res[threadIdx.x] = 0ull;
+    named_sync(1, kConsumers);
+    rank_lists16(clists, C, res, threadIdx.x);
+    named_sync(1, kConsumers);
+    if (threadIdx.x < kCand) {
+      const uint64_t key = res[threadIdx.x];
+      a.out_idx[row * kCand + threadIdx.x] = static_cast<int32_t>(~static_cast<uint32_t>(key));
+      a.out_val[row * kCand + threadIdx.x] = unord_f32(static_cast<uint32_t>(key >> 32));
+    }
+  }
+  pdl_launch_dependents();
+}
+
 struct KernelSetup {
   bool done = false;
   int occ4 = 1, occ2 = 1;
@@ -583,6 +929,12 @@ cudaError_t ensure_setup(int dev, KernelSetup*& out) {
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk16_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_rows_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kRSmemBytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_rows_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kRSmemBytes));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k.occ4, topk16_kernel<4>, kThreads,
                                                       kSmemBytes);
@@ -625,6 +977,27 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
   e = ensure_setup(dev, k);
   if (e != cudaSuccess) return e;
   const DeviceInfo info = device_info();
+  // Few rows: one cluster of C CTAs per row while the clusters fit in about one
+  // wave (two CTAs per SM) and each CTA streams at most kRMaxTilesPerCta tiles.
+  {
+    int C = std::min(kRMaxCluster, plan.tiles_per_row);
+    while (C > 1 && (long long)plan.rows * C > 2LL * info.sms) C >>= 1;
+    if ((long long)plan.rows * C <= 2LL * info.sms &&
+        (plan.tiles_per_row + C - 1) / C <= kRMaxTilesPerCta) {
+      RowsArgs r;
+      r.logits = static_cast<const uint8_t*>(logits);
+      r.V = plan.V;
+      r.tiles_per_row = plan.tiles_per_row;
+      r.C = C;
+      r.out_idx = idx;
+      r.out_val = val;
+      r.err = device_error_word();
+      const dim3 grid(static_cast<unsigned>(plan.rows * C));
+      if (plan.elem_bytes == 4)
+        return launch_kc(topk16_rows_kernel<4>, grid, dim3(kThreads), kRSmemBytes, s, pdl, C, r);
+      return launch_kc(topk16_rows_kernel<8>, grid, dim3(kThreads), kRSmemBytes, s, pdl, C, r);
+    }
+  }
   const int occ = plan.elem_bytes == 4 ? k->occ4 : k->occ2;
   const long long T = (long long)plan.rows * plan.tiles_per_row;
   // One wave of resident CTAs, but no fewer than kMinTilesPerCta tiles per CTA
