@@ -35,6 +35,15 @@ BATCHED = "serving_b64"
 METRIC = "µs per draft block at B=1; blocks/s and HBM GB/s vs roofline at B=64"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the op's
+# kernel from the ncu captures summarised under profiles/, by (op, workload).  An
+# entry is removed when its kernel changes; ops without one report null.
+NCU_TRAFFIC = {
+    ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
+    ("topk", "serving_b64"): 314978816,     # topk16_kernel_serving_b64.md
+    ("conv", "drafter4b_l16"): 1785088,     # conv_small_drafter4b_l16.md
+    ("conv", "serving_b64"): 7273472,       # conv_tc_serving_b64.md
+}
 
 
 # --------------------------------------------------------------------------- bytes
@@ -256,11 +265,12 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
     shares = {"topk": res["topk"]["mean_ms"], "select": res["select"]["mean_ms"],
               "walk": res["walk"]["mean_ms"], "conv": res["conv"]["mean_ms"] * w.conv_calls}
     dominant = max(shares, key=shares.get)
+    tr = lambda op: NCU_TRAFFIC.get((op, w.name))
     per_kernel = {
-        "topk": roofline_obj(tb["topk"], res["topk"]["mean_ms"], peak, which),
-        "select": roofline_obj(tb["select"], res["select"]["mean_ms"], peak, which),
-        "walk": roofline_obj(tb["walk"], res["walk"]["mean_ms"], peak, which),
-        "conv": roofline_obj(cb, res["conv"]["mean_ms"], peak, which),
+        "topk": roofline_obj(tb["topk"], res["topk"]["mean_ms"], peak, which, tr("topk")),
+        "select": roofline_obj(tb["select"], res["select"]["mean_ms"], peak, which, tr("select")),
+        "walk": roofline_obj(tb["walk"], res["walk"]["mean_ms"], peak, which, tr("walk")),
+        "conv": roofline_obj(cb, res["conv"]["mean_ms"], peak, which, tr("conv")),
     }
     per_kernel["select"]["tflops"] = round(select_flops(w) / (res["select"]["mean_ms"] * 1e-3)
                                            / 1e12, 2)

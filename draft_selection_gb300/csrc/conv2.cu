@@ -152,10 +152,13 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       umma_commit(accum_bar);
     }
     __syncwarp();
-  } else if (warp < 4) {  // idle during the mainloop: the base slice for the CTA's channels
+  } else if (warp < 4) {
+    // idle during the mainloop: the base slice for the CTA's channels, stored
+    // [tap][channel within group][group] so that threads on consecutive groups
+    // read consecutive banks in the mix
     for (int e = tid - 64; e < 2 * 16 * NG; e += 64) {
-      const int tap = e / (16 * NG), c = 16 * g0 + e % (16 * NG);
-      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+      const int tap = e / (16 * NG), cl = e % (16 * NG), c = 16 * g0 + cl;
+      bslice[tap * 16 * NG + (cl % 16) * NG + cl / 16] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
     }
   } else {
     // ---- TMEM -> the corrections (one split), or push this split's partial rows
@@ -247,8 +250,8 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       const int r = m0 + r_lo + lr, g = g0 + gl;
       const float c0 = corr[size_t(lr) * pitch + gl];
       const float c1 = corr[size_t(lr) * pitch + NG + gl];
-      const float* b0 = bslice + 16 * gl;
-      const float* b1 = bslice + 16 * NG + 16 * gl;
+      const float* b0 = bslice + gl;            // channel ch at b0[ch * NG]
+      const float* b1 = bslice + 16 * NG + gl;
       uint4 out[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -258,10 +261,10 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int ch = 8 * h + 2 * q;
-          const float lo = fmaf(b0[ch] + c0, __uint_as_float(tw[q] << 16),
-                                (b1[ch] + c1) * __uint_as_float(mw[q] << 16));
-          const float hi = fmaf(b0[ch + 1] + c0, __uint_as_float(tw[q] & 0xFFFF0000u),
-                                (b1[ch + 1] + c1) * __uint_as_float(mw[q] & 0xFFFF0000u));
+          const float lo = fmaf(b0[ch * NG] + c0, __uint_as_float(tw[q] << 16),
+                                (b1[ch * NG] + c1) * __uint_as_float(mw[q] << 16));
+          const float hi = fmaf(b0[(ch + 1) * NG] + c0, __uint_as_float(tw[q] & 0xFFFF0000u),
+                                (b1[(ch + 1) * NG] + c1) * __uint_as_float(mw[q] & 0xFFFF0000u));
           const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
           ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
         }
