@@ -42,7 +42,7 @@ NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
     ("topk", "serving_b64"): 314978816,     # topk16_kernel_serving_b64.md
     ("conv", "drafter4b_l16"): 1785088,     # conv_small_drafter4b_l16.md
-    ("conv", "serving_b64"): 7273472,       # conv_tc_serving_b64.md
+    ("conv", "serving_b64"): 7277056,       # conv_tc_serving_b64.md
 }
 
 

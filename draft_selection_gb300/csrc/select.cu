@@ -19,7 +19,7 @@
 //
 // Stage 2, the pair kernel: one CTA per (sequence, position) forms the 16x16
 // scores from the previous position's A rows, the gate and this position's B
-// rows.  In the fused tail it also takes the walk's decision for each of its
+// rows (2x2 register blocking over 16-byte shared-memory reads).  In the fused tail it also takes the walk's decision for each of its
 // 16 rows, and the last CTA of each sequence follows the chosen slots.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -276,13 +276,22 @@ struct PairArgs {
   float* qrows;             // [B*L][16][16] workspace
 };
 
-// One CTA per (sequence b, position t); thread (i, j) forms S_t(a_i, b_j).
-__global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
-  __shared__ float Gs[kCand][kRank + 1];   // A(a_i) ⊙ H(h_t)
-  __shared__ float Bsh[kCand][kRank + 1];  // B(b_j)
+// One CTA per (sequence b, position t), 128 threads.  The 16x16 dot products
+// of length 256 read shared memory 16 bytes at a time with 2x2 register
+// blocking: thread (half h, ip, jp) forms rows {ip, ip+8} x columns {jp, jp+8}
+// over half h of the rank, and the two halves are added at the end.  Rows sit
+// kPairPitch floats apart (16-byte aligned, and eight consecutive rows fall in
+// different bank groups).
+constexpr int kPairThreads = 128;
+constexpr int kPairPitch = kRank + 4;
+
+__global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
+  __shared__ __align__(16) float Gs[kCand][kPairPitch];   // A(a_i) ⊙ H(h_t)
+  __shared__ __align__(16) float Bsh[kCand][kPairPitch];  // B(b_j)
   __shared__ float Hs[kRank];
   __shared__ float U[kCand];
   __shared__ float Srow[kCand][kCand + 1];
+  __shared__ float Shalf[kCand][kCand + 1];  // the second rank half's partial sums
   __shared__ int path[128];
   __shared__ uint32_t last;
   pdl_wait();
@@ -293,60 +302,72 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
       size_t(b) * (kCand * (a.L - 1) + 1) + (t == 0 ? 0 : 1 + size_t(kCand) * (t - 1));
   const size_t rowB0 = size_t(b) * kCand * a.L + size_t(kCand) * t;
   const int tid = threadIdx.x;
-  {
-    const float g = a.GH[size_t(cell) * kRank + tid];
-    Hs[tid] = 1.0f / (1.0f + expf(-g));
-  }
   // A and B rows: 16 rows x 64 float4 each; all loads issued before any use.
-  float4 va[4], vb[4];
+  float4 va[8], vb[8];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = tid + 256 * k;
+  for (int k = 0; k < 8; ++k) {
+    const int e = tid + kPairThreads * k;
     const int i = e >> 6, q4 = e & 63;
     va[k] = i < npred ? reinterpret_cast<const float4*>(a.PA + (rowA0 + i) * kRank)[q4]
                       : make_float4(0.f, 0.f, 0.f, 0.f);
     vb[k] = reinterpret_cast<const float4*>(a.PB + (rowB0 + i) * kRank)[q4];
   }
+  for (int q = tid; q < kRank; q += kPairThreads) {
+    const float g = a.GH[size_t(cell) * kRank + q];
+    Hs[q] = 1.0f / (1.0f + expf(-g));
+  }
   if (tid < kCand) U[tid] = a.cand_val[size_t(cell) * kCand + tid];
   __syncthreads();  // Hs complete
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e = tid + 256 * k;
+  for (int k = 0; k < 8; ++k) {
+    const int e = tid + kPairThreads * k;
     const int i = e >> 6, c = 4 * (e & 63);
-    Gs[i][c + 0] = va[k].x * Hs[c + 0];
-    Gs[i][c + 1] = va[k].y * Hs[c + 1];
-    Gs[i][c + 2] = va[k].z * Hs[c + 2];
-    Gs[i][c + 3] = va[k].w * Hs[c + 3];
-    Bsh[i][c + 0] = vb[k].x;
-    Bsh[i][c + 1] = vb[k].y;
-    Bsh[i][c + 2] = vb[k].z;
-    Bsh[i][c + 3] = vb[k].w;
+    const float4 h = *reinterpret_cast<const float4*>(&Hs[c]);
+    *reinterpret_cast<float4*>(&Gs[i][c]) =
+        make_float4(va[k].x * h.x, va[k].y * h.y, va[k].z * h.z, va[k].w * h.w);
+    *reinterpret_cast<float4*>(&Bsh[i][c]) = vb[k];
   }
   __syncthreads();
-  const int i = tid / kCand, j = tid % kCand;
-  float s;
-  if (i < npred) {
-    // Four independent partial sums over the quarters of the rank: shorter chains.
-    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
-#pragma unroll 8
-    for (int q = 0; q < kRank / 4; ++q) {
-      p0 = fmaf(Gs[i][q], Bsh[j][q], p0);
-      p1 = fmaf(Gs[i][q + 64], Bsh[j][q + 64], p1);
-      p2 = fmaf(Gs[i][q + 128], Bsh[j][q + 128], p2);
-      p3 = fmaf(Gs[i][q + 192], Bsh[j][q + 192], p3);
+  {
+    const int half = tid >> 6, tt = tid & 63;
+    const int ip = tt >> 3, jp = tt & 7;
+    const int q0 = half * (kRank / 2);
+    float4 s00 = make_float4(0.f, 0.f, 0.f, 0.f), s01 = s00, s10 = s00, s11 = s00;
+#pragma unroll 4
+    for (int q = q0; q < q0 + kRank / 2; q += 4) {
+      const float4 g0 = *reinterpret_cast<const float4*>(&Gs[ip][q]);
+      const float4 g1 = *reinterpret_cast<const float4*>(&Gs[ip + 8][q]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&Bsh[jp][q]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&Bsh[jp + 8][q]);
+      s00.x = fmaf(g0.x, b0.x, s00.x); s00.y = fmaf(g0.y, b0.y, s00.y);
+      s00.z = fmaf(g0.z, b0.z, s00.z); s00.w = fmaf(g0.w, b0.w, s00.w);
+      s01.x = fmaf(g0.x, b1.x, s01.x); s01.y = fmaf(g0.y, b1.y, s01.y);
+      s01.z = fmaf(g0.z, b1.z, s01.z); s01.w = fmaf(g0.w, b1.w, s01.w);
+      s10.x = fmaf(g1.x, b0.x, s10.x); s10.y = fmaf(g1.y, b0.y, s10.y);
+      s10.z = fmaf(g1.z, b0.z, s10.z); s10.w = fmaf(g1.w, b0.w, s10.w);
+      s11.x = fmaf(g1.x, b1.x, s11.x); s11.y = fmaf(g1.y, b1.y, s11.y);
+      s11.z = fmaf(g1.z, b1.z, s11.z); s11.w = fmaf(g1.w, b1.w, s11.w);
     }
-    s = ((p0 + p1) + (p2 + p3)) + U[j];
-  } else {
-    s = -INFINITY;
+    float (*dst)[kCand + 1] = half ? Shalf : Srow;
+    dst[ip][jp] = (s00.x + s00.y) + (s00.z + s00.w);
+    dst[ip][jp + 8] = (s01.x + s01.y) + (s01.z + s01.w);
+    dst[ip + 8][jp] = (s10.x + s10.y) + (s10.z + s10.w);
+    dst[ip + 8][jp + 8] = (s11.x + s11.y) + (s11.z + s11.w);
   }
-  a.scores[size_t(cell) * kCand * kCand + tid] = s;
+  __syncthreads();
+  // S = U_t(b_j) + the two rank halves; rows past the predecessors are -inf
+  for (int e = tid; e < kCand * kCand; e += kPairThreads) {
+    const int i = e / kCand, j = e % kCand;
+    const float v = i < npred ? (Srow[i][j] + Shalf[i][j]) + U[j] : -INFINITY;
+    Srow[i][j] = v;
+    a.scores[size_t(cell) * kCand * kCand + e] = v;
+  }
   if (!a.walk) {
     pdl_launch_dependents();
     return;
   }
 
   // ---- fused walk: the decision of every row of this position ----
-  Srow[i][j] = s;
   __syncthreads();
   if (tid < npred) {
     const float u = a.T > 0.f ? walk_uniform(a.seeds[b], a.cycle, t) : 0.f;
@@ -372,7 +393,7 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
   __threadfence();
   const int* ch = a.choice + size_t(b) * a.L * kCand;
   int* chs = reinterpret_cast<int*>(&Gs[0][0]);  // L x 16 choices (L <= 128 fits)
-  for (int e = tid; e < a.L * kCand; e += 256) chs[e] = __ldcg(ch + e);
+  for (int e = tid; e < a.L * kCand; e += kPairThreads) chs[e] = __ldcg(ch + e);
   __syncthreads();
   if (tid == 0) {
     int prev = 0;
@@ -382,13 +403,13 @@ __global__ void __launch_bounds__(256) pair16_kernel(PairArgs a) {
     }
   }
   __syncthreads();
-  for (int tt = tid; tt < a.L; tt += 256) {
+  for (int tt = tid; tt < a.L; tt += kPairThreads) {
     const size_t c2 = size_t(b) * a.L + tt;
     a.tokens[c2] = a.cand_idx[c2 * kCand + path[tt]];
     if (a.slots) a.slots[c2] = path[tt];
   }
   if (a.q) {
-    for (int e = tid; e < a.L * kCand; e += 256) {
+    for (int e = tid; e < a.L * kCand; e += kPairThreads) {
       const int tt = e / kCand, k = e % kCand;
       const size_t c2 = size_t(b) * a.L + tt;
       const int row = tt == 0 ? 0 : path[tt - 1];  // step tt draws from its predecessor's row
@@ -505,7 +526,7 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
     qa.qrows = reinterpret_cast<float*>(w + p.q_off);
   }
-  return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(256), 0, s, pdl, qa);
+  return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
 }
 
 // ---- tensor maps ------------------------------------------------------------------
