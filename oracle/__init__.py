@@ -65,6 +65,9 @@ def lib():
         L.oracle_walk.restype = I
         L.oracle_conv2.argtypes = [P, P, P, P, I, I, I, P, P]
         L.oracle_conv2.restype = I
+        L.oracle_verify_uniforms.argtypes = [U64, U64, I, P]
+        L.oracle_verify.argtypes = [P, P, P, P, P, I, I, I, I, P, U64, P, P]
+        L.oracle_verify.restype = I
         L.oracle_round_bf16.argtypes = [D]
         L.oracle_round_bf16.restype = ctypes.c_uint16
         _lib = L
@@ -192,3 +195,32 @@ def conv2(x, x_prev, base, W_c):
     if rc != 0:
         raise ValueError("oracle_conv2 rejected its arguments")
     return y, yb
+
+
+def verify_uniforms(seed: int, cycle: int, t: int) -> tuple[float, float]:
+    u = np.zeros(2, np.float64)
+    lib().oracle_verify_uniforms(seed, cycle, t, _ptr(u))
+    return float(u[0]), float(u[1])
+
+
+def verify(p, tokens, slots=None, q=None, cand_idx=None, greedy: bool = True, seeds=None,
+           cycle: int = 0):
+    """p [B, L+1, V] float32 target distributions.  Returns (n_accepted [B] int32,
+    out [B, L+1] int32)."""
+    p = _c(p, np.float32)
+    tokens = _c(tokens, np.int32)
+    B, L = tokens.shape
+    V = p.shape[-1]
+    if p.shape != (B, L + 1, V):
+        raise ValueError("p must be [B, L+1, V]")
+    sl = None if slots is None else _c(slots, np.int32)
+    qq = None if q is None else _c(q, np.float32)
+    ci = None if cand_idx is None else _c(cand_idx, np.int32)
+    sd = None if seeds is None else _c(seeds, np.uint64)
+    n = np.zeros(B, np.int32)
+    out = np.zeros((B, L + 1), np.int32)
+    rc = lib().oracle_verify(_ptr(p), _ptr(tokens), _ptr(sl), _ptr(qq), _ptr(ci), B, L, V,
+                             int(bool(greedy)), _ptr(sd), int(cycle), _ptr(n), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_verify rejected its arguments")
+    return n, out

@@ -312,3 +312,108 @@ int oracle_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
   }
   return bad ? -1 : 0;
 }
+
+/* ---------------------------------------------------------------- verify */
+
+void oracle_verify_uniforms(uint64_t seed, uint64_t cycle, int t, double u[2]) {
+  uint32_t ctr[4] = {(uint32_t)t, (uint32_t)cycle, (uint32_t)(cycle >> 32), 1u};
+  uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+  uint32_t out[4];
+  oracle_philox4x32_10(ctr, key, out);
+  u[0] = (double)(out[0] >> 8) * ldexp(1.0, -24);
+  u[1] = (double)(out[1] >> 8) * ldexp(1.0, -24);
+}
+
+static int32_t row_argmax(const float* row, int V) {
+  int32_t best = 0;
+  for (int v = 1; v < V; ++v)
+    if ((double)row[v] > (double)row[best]) best = v;
+  return best;
+}
+
+/* First v whose running sum of w exceeds target; the last v with w > 0 when
+ * rounding leaves none. */
+static int32_t draw_index(const double* w, int V, double target) {
+  double cum = 0.0;
+  for (int v = 0; v < V; ++v) {
+    cum += w[v];
+    if (target < cum) return v;
+  }
+  for (int v = V - 1; v >= 0; --v)
+    if (w[v] > 0.0) return v;
+  return 0;
+}
+
+int oracle_verify(const float* p, const int32_t* tokens, const int32_t* slots, const float* q,
+                  const int32_t* cand_idx, int B, int L, int V, int greedy,
+                  const uint64_t* seeds, uint64_t cycle, int32_t* n_accepted, int32_t* out) {
+  if (!p || !tokens || !n_accepted || !out || B < 1 || L < 1 || V < 1) return -1;
+  if (!greedy && (!slots || !q || !cand_idx || !seeds)) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int b = 0; b < B; ++b) {
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!w) {
+      bad = 1;
+      continue;
+    }
+    int32_t* o = out + (size_t)b * (L + 1);
+    for (int t = 0; t <= L; ++t) o[t] = -1;
+    int n = L;
+    int32_t emit = -1;
+    for (int t = 0; t < L; ++t) {
+      const float* row = p + ((size_t)b * (L + 1) + t) * V;
+      const int32_t x = tokens[(size_t)b * L + t];
+      if (greedy) {
+        const int32_t a = row_argmax(row, V);
+        if (x == a) {
+          o[t] = x;
+          continue;
+        }
+        n = t;
+        emit = a;
+        break;
+      }
+      double u[2];
+      oracle_verify_uniforms(seeds[b], cycle, t, u);
+      const size_t cell = (size_t)b * L + t;
+      const double qx = (double)q[cell * 16 + slots[cell]];
+      if (u[0] * qx < (double)row[x]) {
+        o[t] = x;
+        continue;
+      }
+      /* rejected: draw from the residual max(0, p - q) */
+      double Z = 0.0;
+      for (int v = 0; v < V; ++v) w[v] = (double)row[v];
+      for (int k = 0; k < 16; ++k) {
+        const int32_t c = cand_idx[cell * 16 + k];
+        if (c >= 0 && c < V) w[c] -= (double)q[cell * 16 + k];
+      }
+      for (int v = 0; v < V; ++v) {
+        if (w[v] < 0.0) w[v] = 0.0;
+        Z += w[v];
+      }
+      if (Z <= 0.0) { /* p does not exceed q anywhere: draw from p itself */
+        for (int v = 0; v < V; ++v) Z += (w[v] = (double)row[v]);
+      }
+      n = t;
+      emit = draw_index(w, V, u[1] * Z);
+      break;
+    }
+    if (n == L) { /* every draft token accepted: one more from row L */
+      const float* row = p + ((size_t)b * (L + 1) + L) * V;
+      if (greedy) {
+        emit = row_argmax(row, V);
+      } else {
+        double u[2], Z = 0.0;
+        oracle_verify_uniforms(seeds[b], cycle, L, u);
+        for (int v = 0; v < V; ++v) Z += (w[v] = (double)row[v]);
+        emit = draw_index(w, V, u[1] * Z);
+      }
+    }
+    n_accepted[b] = n;
+    o[n] = emit;
+    free(w);
+  }
+  return bad ? -1 : 0;
+}

@@ -23,6 +23,15 @@
  *          scores.
  *   [PHILOX] Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
  *          1, 2, 3", SC'11: the Philox4x32-10 bijection.
+ *   [VERIFY] [SEL] "全并行打分与低延迟路径步进" (sampling recovers the target's
+ *          distribution by lossless rejection sampling) and [WALK] "One pass to
+ *          draft, one pass to verify" (the accepted prefix is kept, the first
+ *          miss is replaced by the target's own choice, the rest is dropped;
+ *          greedy output equals the target's own).  The rejection rule is the
+ *          published speculative-sampling step: Leviathan, Kalman, Matias,
+ *          "Fast Inference from Transformers via Speculative Decoding", ICML
+ *          2023, and Chen et al., "Accelerating Large Language Model Decoding
+ *          with Speculative Sampling", 2023.
  *
  * Readings where the pages are silent are stated at each function.
  * bf16 arguments are raw 16-bit patterns (uint16_t); bf16 -> double is exact.
@@ -94,6 +103,32 @@ int oracle_walk(const double* scores, const int32_t* cand_idx, int B, int L, dou
  * even (nullable).  Returns 0, or -1 on a bad argument. */
 int oracle_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
                  const uint16_t* W_c, int B, int L, int d, double* y_exact, uint16_t* y_bf16);
+
+/* The two uniforms verification draws at block position t (reading, the pages
+ * name no generator): words 0 and 1 of Philox4x32-10 with counter
+ * (t, lo32(cycle), hi32(cycle), 1) and key = the sequence's seed, each
+ * (w >> 8) * 2^-24.  u[0] decides acceptance, u[1] the replacement draw. */
+void oracle_verify_uniforms(uint64_t seed, uint64_t cycle, int t, double u[2]);
+
+/* Verification of a drafted block [VERIFY].  p [B, L+1, V] holds the target's
+ * next-token distributions: row t (t < L) follows the verified token and the
+ * first t drafted tokens, row L follows the whole block.  For t = 0..L-1:
+ *   greedy: accept iff tokens[t] is the lowest index holding the row's maximum;
+ *           otherwise emit that index and stop;
+ *   sampling: with x = tokens[t] and its draft probability q(x) =
+ *           q[b,t,slots[t]], accept iff u0 * q(x) < p_t(x); otherwise draw from
+ *           r(v) = max(0, p_t(v) - q_t(v)) (q_t is zero off the 16 candidates
+ *           cand_idx[b,t,:]): the first v, in index order, whose running sum of
+ *           r exceeds u1 * sum(r) (the last v with r > 0 if rounding leaves
+ *           none; p_t itself if sum(r) = 0), emit it and stop.
+ * When all L are accepted, one more token comes from row L (its argmax, or a
+ * draw from p_L with u1 of t = L).  Writes n_accepted [B] (0..L) and out
+ * [B, L+1]: the accepted draft tokens, then the emitted token, then -1.
+ * q, slots, cand_idx and seeds may be NULL when greedy.  Returns 0, or -1 on a
+ * bad argument. */
+int oracle_verify(const float* p, const int32_t* tokens, const int32_t* slots, const float* q,
+                  const int32_t* cand_idx, int B, int L, int V, int greedy,
+                  const uint64_t* seeds, uint64_t cycle, int32_t* n_accepted, int32_t* out);
 
 /* Round a double to the nearest bf16 (ties to even), as a bit pattern. */
 uint16_t oracle_round_bf16(double v);
