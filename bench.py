@@ -283,6 +283,32 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
     return res, g_step
 
 
+def measure_verify(w: wl.Workload, device, steps, warmup, flush, peak_gbs):
+    """Block verification (dfl2_verify) after the walk, each mode in its own
+    graph: sampling reads one row of target probabilities per sequence, greedy
+    ranks all L+1 rows."""
+    import draft_selection_gb300 as dfl2
+    inp = wl.make_verify_inputs(w, device=device)
+    B, L, V = w.B, w.L, w.V
+    n = torch.empty(B, dtype=torch.int32, device=device)
+    out = torch.empty(B, L + 1, dtype=torch.int32, device=device)
+    ws = dfl2.workspace(dfl2.dfl2_verify_workspace_size(B, L, V), device)
+    seeds = torch.from_numpy(inp["seeds"].view(np.int64)).to(device)
+    res = {}
+    for mode in ("sampling", "greedy"):
+        fn = lambda g=(mode == "greedy"): dfl2.dfl2_verify(
+            inp["p"], inp["tokens"], n, out, greedy=g, slots=inp["slots"], q=inp["q"],
+            cand_idx=inp["cand_idx"], seeds=seeds, cycle_offset=0, ws=ws)
+        graph, _ = capture(fn)
+        ms = summarize(time_graph(graph, max(3, min(steps, 200)), warmup, flush))["mean_ms"]
+        nbytes = B * (V * 4 + L * 16) if mode == "sampling" else B * (L + 1) * V * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        res[mode] = {"us": round(ms * 1e3, 2), "bytes": nbytes, "gbs": round(gbs, 1),
+                     "frac_of_hbm": round(gbs / peak_gbs, 4)}
+    del inp
+    return res
+
+
 def measure_e2e(case: Case, g_step, steps, warmup, flush):
     """The same step with the inputs copied from pinned host memory and the
     result read back inside the timed region."""
@@ -474,6 +500,7 @@ def main():
     barrier(world)
     e2e_ms, h2d, d2h = measure_e2e(case, g_step, max(3, min(args.steps, 200)), args.warmup, flush)
     e2e_ms = max_over_ranks(e2e_ms, world)
+    verify = {w.name: measure_verify(w, device, args.steps, args.warmup, flush, pk["hbm_gbs"])}
 
     batched = None
     if args.batched:
@@ -498,6 +525,7 @@ def main():
                           ("topk", "select", "walk", "conv")},
         }
         del cb
+        verify[wb.name] = measure_verify(wb, device, args.steps, args.warmup, flush, pk["hbm_gbs"])
     clk = clocks.stop()
 
     cpu = None
@@ -521,6 +549,7 @@ def main():
             "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
             "per_kernel": res["per_kernel"],
             "b64": batched,
+            "verify": verify,
             "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": "µs per draft block",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": res["kernels_per_step"] * args.steps,

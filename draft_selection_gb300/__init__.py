@@ -65,8 +65,11 @@ def load():
     L.dfl2_tail_workspace_size.restype = SZ
     L.dfl2_tail.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, F, P, U64, P, P, P, P, P, P,
                             P, SZ, P]
+    L.dfl2_verify_workspace_size.argtypes = [I, I, I]
+    L.dfl2_verify_workspace_size.restype = SZ
+    L.dfl2_verify.argtypes = [P, P, P, P, P, I, I, I, I, P, U64, P, P, P, SZ, P]
     for name in ("dfl2_workspace_init", "dfl2_device_error", "dfl2_topk", "dfl2_select",
-                 "dfl2_walk", "dfl2_conv2", "dfl2_tail"):
+                 "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -192,6 +195,23 @@ def dfl2_walk(scores, cand_idx, temperature: float, seeds, cycle_offset: int, to
     _check(load().dfl2_walk(_ptr(scores), _ptr(cand_idx), B, L, float(temperature), _ptr(seeds),
                             int(cycle_offset), _ptr(tokens), _ptr(slots), _ptr(q),
                             _stream(stream)))
+
+
+def dfl2_verify_workspace_size(B: int, L: int, V: int) -> int:
+    return int(load().dfl2_verify_workspace_size(B, L, V))
+
+
+def dfl2_verify(p, tokens, n_accepted, out_tokens, *, greedy: bool, slots=None, q=None,
+                cand_idx=None, seeds=None, cycle_offset: int = 0, ws=None, ws_bytes=None,
+                stream=None, dims=None) -> None:
+    """Verification of drafted tokens [B,L] against target probabilities p [B,L+1,V]:
+    n_accepted [B] and out_tokens [B,L+1] (kept tokens, then the emitted token, then -1)."""
+    B, L1, V = dims if dims is not None else p.shape
+    L = L1 - 1
+    wb = ws_bytes if ws_bytes is not None else (_nbytes(ws) if ws is not None else 0)
+    _check(load().dfl2_verify(_ptr(p), _ptr(tokens), _ptr(slots), _ptr(q), _ptr(cand_idx), B, L,
+                              V, int(bool(greedy)), _ptr(seeds), int(cycle_offset),
+                              _ptr(n_accepted), _ptr(out_tokens), _ptr(ws), wb, _stream(stream)))
 
 
 def dfl2_conv2(x, x_prev, base, W_c, y, stream=None, *, dims=None) -> None:

@@ -317,6 +317,61 @@ dfl2_status dfl2_select(const int32_t* cand_idx, const float* cand_val,
   return DFL2_OK;
 }
 
+// Greedy verification ranks the L+1 target rows with the top-16 kernels; its
+// workspace is their top-16 workspace followed by the ranked indices and values.
+static dfl2::TopkPlan verify_topk_plan(int B, int L, int V) {
+  return dfl2::topk_plan(B * (L + 1), V, 4);
+}
+static size_t verify_idx_off(const dfl2::TopkPlan& plan) {
+  return (plan.ws_bytes + 255) / 256 * 256;
+}
+
+size_t dfl2_verify_workspace_size(int B, int L, int V) {
+  if (B < 1 || L < 1 || V < dfl2::kCand) return 0;
+  const dfl2::TopkPlan plan = verify_topk_plan(B, L, V);
+  const size_t rows = size_t(B) * (L + 1);
+  return verify_idx_off(plan) + (rows * dfl2::kCand * 4 + 255) / 256 * 256 + rows * dfl2::kCand * 4;
+}
+
+dfl2_status dfl2_verify(const float* p, const int32_t* tokens, const int32_t* slots,
+                        const float* q, const int32_t* cand_idx, int B, int L, int V, int greedy,
+                        const uint64_t* seeds, uint64_t cycle_offset, int32_t* n_accepted,
+                        int32_t* out_tokens, void* ws, size_t ws_bytes, dfl2_stream stream) {
+  DFL2_TRY(check_shape(B, L));
+  DFL2_TRY(check_block_len(L));
+  if (V < dfl2::kCand) return fail(DFL2_ERR_INVALID_ARG, "V=%d < 16", V);
+  if (V % 4 != 0) return fail(DFL2_ERR_UNSUPPORTED, "V=%d: rows of p must be a multiple of 16 bytes", V);
+  if (V > 524288) return fail(DFL2_ERR_UNSUPPORTED, "V=%d: verification supports V <= 524288", V);
+  const bool sampling = greedy == 0;
+  const Ptrs ptrs = {{p, "p"}, {tokens, "tokens"}, {slots, "slots", !sampling},
+                     {q, "q", !sampling}, {cand_idx, "cand_idx", !sampling},
+                     {seeds, "seeds", !sampling}, {n_accepted, "n_accepted"},
+                     {out_tokens, "out_tokens"}};
+  DFL2_TRY(check_host(ptrs));
+  const dfl2::TopkPlan plan = verify_topk_plan(B, L, V);
+  if (!sampling) DFL2_TRY(check_ws(ws, ws_bytes, dfl2_verify_workspace_size(B, L, V)));
+  DFL2_TRY(ensure_device());
+  DFL2_TRY(check_device(ptrs));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (sampling) {
+    cudaError_t e = dfl2::launch_verify_sample(p, tokens, slots, q, cand_idx, B, L, V, seeds,
+                                               cycle_offset, n_accepted, out_tokens, s);
+    if (e != cudaSuccess) return cuda_fail(e, "verification launch");
+    return DFL2_OK;
+  }
+  DFL2_TRY(check_device_ptr(ws, "workspace"));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const size_t rows = size_t(B) * (L + 1);
+  int32_t* top_idx = reinterpret_cast<int32_t*>(w + verify_idx_off(plan));
+  float* top_val = reinterpret_cast<float*>(w + verify_idx_off(plan) +
+                                            (rows * dfl2::kCand * 4 + 255) / 256 * 256);
+  cudaError_t e = dfl2::launch_topk(plan, p, top_idx, top_val, ws, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "verification top-16 launch");
+  e = dfl2::launch_verify_greedy(tokens, top_idx, B, L, n_accepted, out_tokens, s);
+  if (e != cudaSuccess) return cuda_fail(e, "verification launch");
+  return DFL2_OK;
+}
+
 dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L,
                       float temperature, const uint64_t* seeds, uint64_t cycle_offset,
                       int32_t* tokens, int32_t* slots, float* q, dfl2_stream stream) {

@@ -180,6 +180,13 @@ struct TopkPlan {
   size_t ws_bytes;
 };
 TopkPlan topk_plan(int rows, int V, int elem_bytes);
+// Block verification (verify.cu).
+cudaError_t launch_verify_sample(const float* p, const int32_t* tokens, const int32_t* slots,
+                                 const float* q, const int32_t* cand_idx, int B, int L, int V,
+                                 const uint64_t* seeds, uint64_t cycle, int32_t* n_accepted,
+                                 int32_t* out, cudaStream_t s);
+cudaError_t launch_verify_greedy(const int32_t* tokens, const int32_t* top_idx, int B, int L,
+                                 int32_t* n_accepted, int32_t* out, cudaStream_t s);
 cudaError_t launch_topk(const TopkPlan& p, const void* logits, int32_t* idx, float* val,
                         void* ws, cudaStream_t s, bool pdl);
 
@@ -445,6 +452,24 @@ __device__ __forceinline__ uint32_t philox4x32_10_w0(uint32_t c0, uint32_t c1, u
     k1 += 0xBB67AE85u;
   }
   return c0;
+}
+
+// Philox4x32-10, words 0 and 1 of the output block.
+__device__ __forceinline__ uint2 philox4x32_10_w01(uint32_t c0, uint32_t c1, uint32_t c2,
+                                                   uint32_t c3, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return make_uint2(c0, c1);
 }
 
 // Uniform in [0,1) of step t: counter (t, lo32(cycle), hi32(cycle), 0), key = seed.

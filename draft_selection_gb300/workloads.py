@@ -142,6 +142,39 @@ def make_conv_inputs(w: Workload, call: int, device="cpu") -> dict:
     return out
 
 
+def make_verify_inputs(w: Workload, device="cpu", temperature: float = 1.0,
+                       sharp: float = 3.0) -> dict:
+    """Synthetic inputs for block verification.  p [B, L+1, V] float32: the
+    target's next-token distributions, softmax of `sharp` times a target logit
+    field that agrees with the drafter's logits up to N(0, 1) noise (row L is a
+    fresh field); `sharp` sets how much mass the top candidates hold, and so
+    the spread of accepted lengths.  The draft side is drawn independently of any kernel: 16 distinct
+    candidates per position sampled from p without replacement, a draft
+    distribution q over them (the target's probabilities on the candidates,
+    perturbed by N(0, 0.5) in log space, renormalised, at the temperature), and
+    the slot (and so the token) drawn from q."""
+    B, L, V = w.B, w.L, w.V
+    g = _generator(w, "verify.noise", device)
+    lg = make_logits(w, device).float()
+    tgt = torch.empty(B, L + 1, V, device=device)
+    tgt[:, :L] = lg + torch.randn(B, L, V, generator=g, device=device)
+    tgt[:, L] = 2.0 * torch.randn(B, V, generator=g, device=device)
+    p = torch.softmax(sharp * tgt, dim=-1)
+    g = _generator(w, "verify.cand", device)
+    cand = torch.multinomial(p[:, :L].reshape(B * L, V), 16, replacement=False, generator=g)
+    g = _generator(w, "verify.q", device)
+    pc = torch.gather(p[:, :L].reshape(B * L, V), 1, cand)
+    noise = 0.5 * torch.randn(B * L, 16, generator=g, device=device)
+    q = torch.softmax((torch.log(pc) + noise) / max(temperature, 1e-3), dim=-1)
+    g = _generator(w, "verify.slot", device)
+    slots = torch.multinomial(q, 1, generator=g).view(B, L)
+    cand = cand.view(B, L, 16).to(torch.int32)
+    tokens = torch.gather(cand, 2, slots.view(B, L, 1).long()).view(B, L).to(torch.int32)
+    return {"p": p.contiguous(), "cand_idx": cand, "q": q.view(B, L, 16).contiguous(),
+            "slots": slots.to(torch.int32), "tokens": tokens,
+            "seeds": philox_seeds(w, salt=7)}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """A bf16 tensor's bit patterns as a host uint16 array (what the oracle takes)."""
     assert t.dtype == torch.bfloat16

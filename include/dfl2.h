@@ -183,6 +183,53 @@ dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verif
                       float* cand_val, float* scores, void* ws, size_t ws_bytes,
                       dfl2_stream stream);
 
+/* ---------------------------------------------------------------------------
+ * dfl2_verify: verification of the drafted block against the target's
+ * distributions, the step after the walk ("DFlash 2: Keep Drafting Parallel",
+ * 方法细节 > 轻量级路径选择器, "全并行打分与低延迟路径步进": lossless rejection
+ * sampling recovers the target's distribution; "DFlash 2: The Drafter Stopped
+ * Guessing Alone", "One pass to draft, one pass to verify": the accepted prefix
+ * is kept, the first miss is replaced by the target's own choice and the rest
+ * dropped).  The sampling rule is the published speculative-sampling step
+ * (Leviathan et al., ICML 2023; Chen et al., 2023).
+ *
+ *   p          [B, L+1, V] float32, device: the target's next-token
+ *              probabilities; row t < L follows the verified token and the first
+ *              t drafted tokens, row L follows the whole block.
+ *   tokens     [B, L] int32: the drafted tokens (dfl2_walk / dfl2_tail).
+ *   greedy     non-zero: keep tokens[t] while it is the lowest index holding the
+ *              maximum of row t; the first miss is replaced by that index; when
+ *              all L match, row L's argmax is appended.
+ *              zero (sampling): with x = tokens[t] and q(x) = q[b,t,slots[t]],
+ *              keep x iff u0 * q(x) < p_t(x); otherwise draw the replacement
+ *              from max(0, p_t - q_t) (q_t is zero off cand_idx[b,t,:]): the
+ *              first index, in order, whose running sum exceeds u1 * total (the
+ *              last index with mass if rounding leaves none; p_t itself if the
+ *              residual is zero).  When all L are kept, one token is drawn from
+ *              row L the same way with u1.  u0, u1 = words 0 and 1 of
+ *              Philox4x32-10 with counter (t, lo32(cycle), hi32(cycle), 1) and
+ *              key = seeds[b], each (w >> 8) * 2^-24.
+ *   slots, q, cand_idx, seeds: the walk's outputs [B,L], [B,L,16], the top-16
+ *              candidates [B,L,16] and the per-sequence keys [B]; unused (may
+ *              be NULL) when greedy.
+ *   n_accepted [B] int32: drafted tokens kept (0..L).
+ *   out_tokens [B, L+1] int32: the kept tokens, then the replacement or
+ *              appended token, then -1.
+ *   ws, ws_bytes: dfl2_verify_workspace_size(B, L, V) bytes of device memory
+ *              (used by greedy; sampling may pass NULL and 0).
+ * Constraints: L <= 128, 16 <= V <= 524288, V % 4 == 0.  Decisions are exact
+ * (double precision); the replacement draw sums the row in single precision
+ * within 512-element tiles and in double across tiles, so it can differ from
+ * an exact sum only when u1 * total lies within rounding of a boundary.
+ * Errors: DFL2_ERR_INVALID_ARG / UNSUPPORTED before any launch; a token or
+ * slot out of range is recorded in the device error word (dfl2_device_error).
+ * ------------------------------------------------------------------------- */
+size_t dfl2_verify_workspace_size(int B, int L, int V);
+dfl2_status dfl2_verify(const float* p, const int32_t* tokens, const int32_t* slots,
+                        const float* q, const int32_t* cand_idx, int B, int L, int V, int greedy,
+                        const uint64_t* seeds, uint64_t cycle_offset, int32_t* n_accepted,
+                        int32_t* out_tokens, void* ws, size_t ws_bytes, dfl2_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

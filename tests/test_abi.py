@@ -31,7 +31,7 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail"):
+    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify"):
         assert n in names
 
 
@@ -86,6 +86,23 @@ def test_walk_rejects_bad_arguments(lib):
     assert f(A, A, 1, 8, 1.0, A, 0, None, None, None, None) == INVALID        # no tokens
     assert f(A, A, 1, 8, 1.0, A, 0, A, A + 4, None, None) == INVALID          # misaligned slots
     assert f(A, A, 0, 8, 0.0, None, 0, A, None, None, None) == INVALID        # B = 0
+
+
+def test_verify_rejects_bad_arguments(lib):
+    f = lib.dfl2_verify
+    ws = dfl2.dfl2_verify_workspace_size(1, 8, 1024)
+    assert ws > 0
+    # greedy: slots, q, cand_idx and seeds may be NULL; the workspace is required
+    assert f(A, A2, None, None, None, 1, 8, 1024, 1, None, 0, A, A, A, 0, None) == WORKSPACE
+    assert f(A, A2, None, None, None, 1, 8, 1022, 1, None, 0, A, A, A, ws, None) == UNSUPPORTED  # V % 4
+    assert f(A, A2, None, None, None, 1, 8, 8, 1, None, 0, A, A, A, ws, None) == INVALID         # V < 16
+    assert f(A, A2, None, None, None, 1, 200, 1024, 1, None, 0, A, A, A, ws, None) == UNSUPPORTED  # L > 128
+    assert f(A, A2, None, None, None, 1, 8, 1 << 20, 1, None, 0, A, A, A, ws, None) == UNSUPPORTED  # V too big
+    assert f(None, A2, None, None, None, 1, 8, 1024, 1, None, 0, A, A, A, ws, None) == INVALID   # NULL p
+    # sampling needs the walk's outputs and the keys
+    assert f(A, A2, None, A, A, 1, 8, 1024, 0, A, 0, A, A, None, 0, None) == INVALID   # no slots
+    assert f(A, A2, A, A, A, 1, 8, 1024, 0, None, 0, A, A, None, 0, None) == INVALID   # no seeds
+    assert f(A, A2, A, A + 4, A, 1, 8, 1024, 0, A, 0, A, A, None, 0, None) == INVALID  # misaligned q
 
 
 def test_conv_rejects_bad_arguments(lib):
