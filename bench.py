@@ -60,6 +60,17 @@ def tail_bytes(w: wl.Workload, es: int) -> dict:
     return {"topk": topk, "select": select, "walk": walk, "total": topk + select + walk}
 
 
+def tail_tables_bytes(w: wl.Workload, es: int) -> int:
+    """Algorithmic HBM bytes of one table tail: logits, the gathered table rows
+    (A rows of the predecessors, B rows of the candidates, float32), hidden,
+    W_H and the outputs."""
+    R = w.rows
+    rows_a = w.B * (16 * (w.L - 1) + 1)
+    rows_b = w.B * 16 * w.L
+    return (R * w.V * es + (rows_a + rows_b) * 256 * 4 + R * w.d * 2 + 256 * w.d * 2
+            + w.B * 4 + R * 16 * 8 + R * 4 + R * 16 * 4)
+
+
 def conv_bytes(w: wl.Workload) -> int:
     d = w.d
     return (2 * w.B * w.L * d * 2 + w.B * d * 2 + 2 * d * 4 + (2 * d // 16) * d * 2)
@@ -192,6 +203,26 @@ class Case:
     def walk(self):
         self.dfl2.dfl2_walk(self.scores, self.idx, self.T, self.seeds, 0, self.tokens, q=self.q)
 
+    def build_tables(self):
+        """P_A, P_B (float32 [V,256]) for the table variant; returns the build time (ms)."""
+        V = self.w.V
+        dev = self.logits.device
+        self.PA = torch.empty(V, 256, dtype=torch.float32, device=dev)
+        self.PB = torch.empty_like(self.PA)
+        i = self.inp
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        self.dfl2.dfl2_tables_build(i["E"], i["W_A"], i["W_B"], self.PA, self.PB)  # warm
+        a.record()
+        self.dfl2.dfl2_tables_build(i["E"], i["W_A"], i["W_B"], self.PA, self.PB)
+        b.record()
+        b.synchronize()
+        return a.elapsed_time(b)
+
+    def tail_tables(self):
+        i = self.inp
+        self.dfl2.dfl2_tail_tables(self.logits, i["verified"], i["hidden"], i["W_H"], self.PA,
+                                   self.PB, self.T, self.seeds, 0, self.tokens, self.ws, q=self.q)
+
 
 def capture(fn):
     """CUDA graph of fn (warmed up twice first); returns (graph, kernels per replay)."""
@@ -261,6 +292,14 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
            "walk": summarize(time_graph(g_walk, sub, warmup, flush)),
            "conv": summarize(time_graph(g_conv, sub, warmup, flush))}
     res["kernels_per_step"] = k_step
+    build_ms = case.build_tables()
+    g_tt, _ = capture(case.tail_tables)
+    tt = summarize(time_graph(g_tt, sub, warmup, flush))["mean_ms"]
+    ttb = tail_tables_bytes(w, case.es)
+    res["tables"] = {"tail_us": round(tt * 1e3, 2), "build_ms": round(build_ms, 3),
+                     "tail_bytes": ttb,
+                     "tail_frac_of_hbm": round(ttb / (tt * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+    del case.PA, case.PB
     peak = pk["hbm_gbs"]
     shares = {"topk": res["topk"]["mean_ms"], "select": res["select"]["mean_ms"],
               "walk": res["walk"]["mean_ms"], "conv": res["conv"]["mean_ms"] * w.conv_calls}
@@ -523,6 +562,7 @@ def main():
             "per_kernel": rb["per_kernel"],
             "kernel_ms": {k: round(rb[k]["mean_ms"], 5) for k in
                           ("topk", "select", "walk", "conv")},
+            "tables": rb["tables"],
         }
         del cb
         verify[wb.name] = measure_verify(wb, device, args.steps, args.warmup, flush, pk["hbm_gbs"])
@@ -548,6 +588,7 @@ def main():
                           ("topk", "select", "walk", "conv")},
             "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
             "per_kernel": res["per_kernel"],
+            "tables": res["tables"],
             "b64": batched,
             "verify": verify,
             "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": "µs per draft block",

@@ -65,11 +65,18 @@ def load():
     L.dfl2_tail_workspace_size.restype = SZ
     L.dfl2_tail.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, F, P, U64, P, P, P, P, P, P,
                             P, SZ, P]
+    L.dfl2_tables_bytes.argtypes = [I]
+    L.dfl2_tables_bytes.restype = SZ
+    L.dfl2_tables_build.argtypes = [P, P, P, I, I, P, P, P]
+    L.dfl2_select_tables.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]
+    L.dfl2_tail_tables.argtypes = [P, I, P, P, P, P, P, I, I, I, I, F, P, U64, P, P, P, P, P, P,
+                                   P, SZ, P]
     L.dfl2_verify_workspace_size.argtypes = [I, I, I]
     L.dfl2_verify_workspace_size.restype = SZ
     L.dfl2_verify.argtypes = [P, P, P, P, P, I, I, I, I, P, U64, P, P, P, SZ, P]
     for name in ("dfl2_workspace_init", "dfl2_device_error", "dfl2_topk", "dfl2_select",
-                 "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify"):
+                 "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify", "dfl2_tables_build",
+                 "dfl2_select_tables", "dfl2_tail_tables"):
         getattr(L, name).restype = I
     _lib = L
     return _lib
@@ -237,3 +244,47 @@ def dfl2_tail(logits, verified_tok, hidden, E, W_A, W_B, W_H, temperature: float
                             _ptr(seeds), int(cycle_offset), _ptr(tokens), _ptr(slots), _ptr(q),
                             _ptr(cand_idx), _ptr(cand_val), _ptr(scores), _ptr(ws), wb,
                             _stream(stream)))
+
+
+def dfl2_tables_bytes(V: int) -> int:
+    return int(load().dfl2_tables_bytes(V))
+
+
+def dfl2_tables_build(E, W_A, W_B, P_A, P_B, stream=None, *, dims=None) -> None:
+    """P_A = E W_A^T, P_B = E W_B^T (float32 [V, 256]), once per set of weights."""
+    V, d = dims if dims is not None else E.shape
+    _check(load().dfl2_tables_build(_ptr(E), _ptr(W_A), _ptr(W_B), V, d, _ptr(P_A), _ptr(P_B),
+                                    _stream(stream)))
+
+
+def dfl2_select_tables(cand_idx, cand_val, verified_tok, hidden, W_H, P_A, P_B, scores, ws,
+                       stream=None, *, dims=None, ws_bytes=None) -> None:
+    """Pair scores [B,L,16,16] with A(.) and B(.) from the token tables."""
+    if dims is not None:
+        B, L, V, d = dims
+    else:
+        B, L, d = hidden.shape
+        V = P_A.shape[0]
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check(load().dfl2_select_tables(_ptr(cand_idx), _ptr(cand_val), _ptr(verified_tok),
+                                     _ptr(hidden), _ptr(W_H), _ptr(P_A), _ptr(P_B), B, L, V, d,
+                                     256, _ptr(scores), _ptr(ws), wb, _stream(stream)))
+
+
+def dfl2_tail_tables(logits, verified_tok, hidden, W_H, P_A, P_B, temperature: float, seeds,
+                     cycle_offset: int, tokens, ws, slots=None, q=None, cand_idx=None,
+                     cand_val=None, scores=None, stream=None, *, dims=None, dtype=None,
+                     ws_bytes=None) -> None:
+    """dfl2_tail with the token tables (the gate projection beside the top-16)."""
+    if dims is not None:
+        B, L, V, d = dims
+    else:
+        B, L, V = logits.shape
+        d = hidden.shape[-1]
+    dt = dtype if dtype is not None else _dtype_code(logits)
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check(load().dfl2_tail_tables(_ptr(logits), dt, _ptr(verified_tok), _ptr(hidden), _ptr(W_H),
+                                   _ptr(P_A), _ptr(P_B), B, L, V, d, float(temperature),
+                                   _ptr(seeds), int(cycle_offset), _ptr(tokens), _ptr(slots),
+                                   _ptr(q), _ptr(cand_idx), _ptr(cand_val), _ptr(scores),
+                                   _ptr(ws), wb, _stream(stream)))

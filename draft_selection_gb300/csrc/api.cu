@@ -317,6 +317,123 @@ dfl2_status dfl2_select(const int32_t* cand_idx, const float* cand_val,
   return DFL2_OK;
 }
 
+// ---- precomputed token tables --------------------------------------------------
+
+size_t dfl2_tables_bytes(int V) {
+  if (V < dfl2::kCand) return 0;
+  return size_t(V) * dfl2::kRank * 4;
+}
+
+dfl2_status dfl2_tables_build(const uint16_t* E, const uint16_t* W_A, const uint16_t* W_B, int V,
+                              int d, float* P_A, float* P_B, dfl2_stream stream) {
+  DFL2_TRY(check_select_args(1, 1, V, d, dfl2::kRank));
+  const Ptrs ptrs = {{E, "E"}, {W_A, "W_A"}, {W_B, "W_B"}, {P_A, "P_A"}, {P_B, "P_B"}};
+  DFL2_TRY(check_host(ptrs));
+  DFL2_TRY(ensure_device());
+  DFL2_TRY(check_device(ptrs));
+  cudaError_t e = dfl2::launch_tables_build(bf(E), bf(W_A), bf(W_B), V, d, P_A, P_B,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "token table launch");
+  return DFL2_OK;
+}
+
+dfl2_status dfl2_select_tables(const int32_t* cand_idx, const float* cand_val,
+                               const int32_t* verified_tok, const uint16_t* hidden,
+                               const uint16_t* W_H, const float* P_A, const float* P_B, int B,
+                               int L, int V, int d, int r, float* scores, void* ws,
+                               size_t ws_bytes, dfl2_stream stream) {
+  DFL2_TRY(check_select_args(B, L, V, d, r));
+  const dfl2::SelectPlan plan = dfl2::select_plan(B, L, d);
+  const Ptrs ptrs = {{cand_idx, "cand_idx"}, {cand_val, "cand_val"}, {verified_tok, "verified_tok"},
+                     {hidden, "hidden"}, {W_H, "W_H"}, {P_A, "P_A"}, {P_B, "P_B"},
+                     {scores, "scores"}};
+  DFL2_TRY(check_host(ptrs));
+  DFL2_TRY(check_ws(ws, ws_bytes, plan.ws_bytes));
+  DFL2_TRY(ensure_device());
+  DFL2_TRY(check_device(ptrs));
+  DFL2_TRY(check_device_ptr(ws, "workspace"));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dfl2::launch_gate(plan, bf(hidden), bf(W_H), ws, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "gate projection launch");
+  e = dfl2::launch_pair_tables(plan, cand_idx, cand_val, verified_tok, P_A, P_B, V, scores,
+                               nullptr, ws, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "pair score launch");
+  return DFL2_OK;
+}
+
+namespace {
+// A side stream and two events per device for each host thread: the table
+// tail runs the gate projection beside the top-16 (they share no data).
+struct SideStream {
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+thread_local SideStream t_side[64];
+
+cudaError_t side_stream(SideStream*& out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  SideStream& ss = t_side[dev & 63];
+  if (!ss.side) {
+    e = cudaStreamCreateWithFlags(&ss.side, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreateWithFlags(&ss.fork, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    e = cudaEventCreateWithFlags(&ss.join, cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+  }
+  out = &ss;
+  return cudaSuccess;
+}
+}  // namespace
+
+dfl2_status dfl2_tail_tables(const void* logits, dfl2_dtype dtype, const int32_t* verified_tok,
+                             const uint16_t* hidden, const uint16_t* W_H, const float* P_A,
+                             const float* P_B, int B, int L, int V, int d, float temperature,
+                             const uint64_t* seeds, uint64_t cycle_offset, int32_t* tokens,
+                             int32_t* slots, float* q, int32_t* cand_idx, float* cand_val,
+                             float* scores, void* ws, size_t ws_bytes, dfl2_stream stream) {
+  DFL2_TRY(check_topk_args(dtype, B, L, V, dfl2::kCand));
+  DFL2_TRY(check_select_args(B, L, V, d, dfl2::kRank));
+  DFL2_TRY(check_block_len(L));
+  DFL2_TRY(check_temperature(temperature));
+  const int es = dtype == DFL2_F32 ? 4 : 2;
+  const TailLayout t = tail_layout(B, L, V, d, es);
+  const Ptrs ptrs = {{logits, "logits"}, {verified_tok, "verified_tok"}, {hidden, "hidden"},
+                     {W_H, "W_H"}, {P_A, "P_A"}, {P_B, "P_B"},
+                     {tokens, "tokens"}, {slots, "slots", true}, {q, "q", true},
+                     {cand_idx, "cand_idx", true}, {cand_val, "cand_val", true},
+                     {scores, "scores", true}, {seeds, "seeds", !(temperature > 0.f)}};
+  DFL2_TRY(check_host(ptrs));
+  DFL2_TRY(check_ws(ws, ws_bytes, t.bytes));
+  DFL2_TRY(ensure_device());
+  DFL2_TRY(check_device(ptrs));
+  DFL2_TRY(check_device_ptr(ws, "workspace"));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* idx = cand_idx ? cand_idx : reinterpret_cast<int32_t*>(w + t.idx_off);
+  float* val = cand_val ? cand_val : reinterpret_cast<float*>(w + t.val_off);
+  float* S = scores ? scores : reinterpret_cast<float*>(w + t.scores_off);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  SideStream* ss = nullptr;
+  cudaError_t e = side_stream(ss);
+  if (e != cudaSuccess) return cuda_fail(e, "side stream");
+  // fork: the gate projection on the side stream, the top-16 on the caller's
+  if ((e = cudaEventRecord(ss->fork, s)) != cudaSuccess) return cuda_fail(e, "fork");
+  if ((e = cudaStreamWaitEvent(ss->side, ss->fork, 0)) != cudaSuccess) return cuda_fail(e, "fork");
+  e = dfl2::launch_gate(t.sel, bf(hidden), bf(W_H), w + t.sel_off, ss->side, false);
+  if (e != cudaSuccess) return cuda_fail(e, "gate projection launch");
+  if ((e = cudaEventRecord(ss->join, ss->side)) != cudaSuccess) return cuda_fail(e, "join");
+  e = dfl2::launch_topk(t.topk, logits, idx, val, w + t.topk_off, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "top-16 launch");
+  if ((e = cudaStreamWaitEvent(s, ss->join, 0)) != cudaSuccess) return cuda_fail(e, "join");
+  const dfl2::WalkFuse wf{temperature, seeds, cycle_offset, tokens, slots, q};
+  e = dfl2::launch_pair_tables(t.sel, idx, val, verified_tok, P_A, P_B, V, S, &wf,
+                               w + t.sel_off, s, true);
+  if (e != cudaSuccess) return cuda_fail(e, "pair score + walk launch");
+  return DFL2_OK;
+}
+
 // Greedy verification ranks the L+1 target rows with the top-16 kernels; its
 // workspace is their top-16 workspace followed by the ranked indices and values.
 static dfl2::TopkPlan verify_topk_plan(int B, int L, int V) {

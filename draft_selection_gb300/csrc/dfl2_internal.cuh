@@ -209,6 +209,21 @@ struct SelectPlan {
   size_t ws_bytes;
 };
 SelectPlan select_plan(int B, int L, int d);
+// Precomputed token tables P_A = E W_A^T, P_B = E W_B^T (float32 [V][256]).
+cudaError_t launch_tables_build(const __nv_bfloat16* E, const __nv_bfloat16* W_A,
+                                const __nv_bfloat16* W_B, int V, int d, float* P_A, float* P_B,
+                                cudaStream_t s);
+// Forward declaration for the table-mode launchers below.
+struct WalkFuse;
+// The gate projection GH = W_H h (before the sigmoid) into the plan's workspace.
+cudaError_t launch_gate(const SelectPlan& p, const __nv_bfloat16* hidden, const __nv_bfloat16* W_H,
+                        void* ws, cudaStream_t s, bool pdl);
+// Pair scores (and, with walk, the fused walk) reading A(.) and B(.) rows from
+// the tables by token; GH must be in the workspace.
+cudaError_t launch_pair_tables(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
+                               const int32_t* verified, const float* P_A, const float* P_B, int V,
+                               float* scores, const WalkFuse* walk, void* ws, cudaStream_t s,
+                               bool pdl);
 // The walk, when it runs inside the pair kernel (the fused tail).
 struct WalkFuse {
   float T;

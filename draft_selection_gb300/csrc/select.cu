@@ -43,7 +43,7 @@ constexpr size_t kGemmSmem = 1024 + size_t(kGStages) * (kAStage + kBStage) + 256
 
 constexpr uint32_t kTmemCols = 256;
 
-enum RowKind : int { kRowsPA = 0, kRowsPB = 1, kRowsHidden = 2 };
+enum RowKind : int { kRowsPA = 0, kRowsPB = 1, kRowsHidden = 2, kRowsE = 3 };
 
 struct GemmProblem {
   int kind;     // RowKind
@@ -69,6 +69,7 @@ struct GemmArgs {
 __device__ __forceinline__ const __nv_bfloat16* a_row(const GemmArgs& a, int kind, int m, int M) {
   if (m >= M) return nullptr;
   if (kind == kRowsHidden) return a.hidden + size_t(m) * a.d;
+  if (kind == kRowsE) return a.E + size_t(m) * a.d;  // the table build: every row of E in order
   int32_t tok;
   if (kind == kRowsPA) {
     const int per = kCand * (a.L - 1) + 1;
@@ -256,8 +257,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 struct PairArgs {
-  const float* PA;  // [MA][256]
+  const float* PA;  // [MA][256] (per-cycle projections), or
   const float* PB;  // [MB][256]
+  const float* tabA;        // [V][256] precomputed A(.) for every token (table mode), or null
+  const float* tabB;        // [V][256] precomputed B(.)
+  const int32_t* verified;  // [B] (table mode)
+  int V;
+  uint32_t* err;
   const float* GH;  // [B*L][256], pre-sigmoid
   const float* cand_val;  // [B,L,16]
   float* scores;          // [B,L,16,16]
@@ -302,15 +308,41 @@ __global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
       size_t(b) * (kCand * (a.L - 1) + 1) + (t == 0 ? 0 : 1 + size_t(kCand) * (t - 1));
   const size_t rowB0 = size_t(b) * kCand * a.L + size_t(kCand) * t;
   const int tid = threadIdx.x;
+  // Row sources: the per-cycle projections, or (table mode) the precomputed
+  // rows of the predecessor and candidate tokens.
+  __shared__ const float* rowA[kCand];
+  __shared__ const float* rowB[kCand];
+  if (tid < 2 * kCand) {
+    const int i = tid % kCand;
+    const bool isA = tid < kCand;
+    const float* src;
+    if (a.tabA) {
+      int tok = 0;
+      if (isA) {
+        if (i < npred)
+          tok = t == 0 ? a.verified[b] : a.cand_idx[(size_t(b) * a.L + (t - 1)) * kCand + i];
+      } else {
+        tok = a.cand_idx[(size_t(b) * a.L + t) * kCand + i];
+      }
+      if (tok < 0 || tok >= a.V) {  // never read outside the tables
+        record_error(a.err, kDevErrBadIndex);
+        tok = 0;
+      }
+      src = (isA ? a.tabA : a.tabB) + size_t(tok) * kRank;
+    } else {
+      src = isA ? a.PA + (rowA0 + i) * kRank : a.PB + (rowB0 + i) * kRank;
+    }
+    (isA ? rowA : rowB)[i] = src;
+  }
+  __syncthreads();
   // A and B rows: 16 rows x 64 float4 each; all loads issued before any use.
   float4 va[8], vb[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int e = tid + kPairThreads * k;
     const int i = e >> 6, q4 = e & 63;
-    va[k] = i < npred ? reinterpret_cast<const float4*>(a.PA + (rowA0 + i) * kRank)[q4]
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    vb[k] = reinterpret_cast<const float4*>(a.PB + (rowB0 + i) * kRank)[q4];
+    va[k] = i < npred ? reinterpret_cast<const float4*>(rowA[i])[q4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    vb[k] = reinterpret_cast<const float4*>(rowB[i])[q4];
   }
   for (int q = tid; q < kRank; q += kPairThreads) {
     const float g = a.GH[size_t(cell) * kRank + q];
@@ -423,6 +455,18 @@ bool g_gemm_attr[64];
 
 }  // namespace
 
+// K split of the gate projection run alone (the table path): the largest power
+// of two <= 8 that keeps its tiles within one wave, every split non-empty.
+static void gate_split(int MH, int kblocks, int& splits, int& kps) {
+  const int tiles = (MH + kBM - 1) / kBM;
+  splits = 1;
+  while (splits * 2 <= kMaxClusterSplits && tiles * splits * 2 <= kGemmTargetCtas &&
+         splits * 2 <= kblocks)
+    splits *= 2;
+  kps = (kblocks + splits - 1) / splits;
+  splits = (kblocks + kps - 1) / kps;
+}
+
 SelectPlan select_plan(int B, int L, int d) {
   SelectPlan p{};
   p.B = B;
@@ -445,13 +489,78 @@ SelectPlan select_plan(int B, int L, int d) {
   p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
   p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);
   p.part_off = align_up(p.GH_off + size_t(p.MH) * kRank * 4, 256);
-  const size_t part_bytes = p.splits > 1 ? size_t(p.splits) * (p.MA + p.MB + p.MH) * kRank * 4 : 0;
+  // split-K partials: of the three problems together, or of the gate alone
+  // (the table path runs the gate projection by itself, with its own split)
+  int gs, gk;
+  gate_split(p.MH, p.kblocks, gs, gk);
+  const size_t part_bytes = std::max(
+      p.splits > 1 ? size_t(p.splits) * (p.MA + p.MB + p.MH) * kRank * 4 : size_t(0),
+      gs > 1 ? size_t(gs) * p.MH * kRank * 4 : size_t(0));
   p.ticket_off = align_up(p.part_off + part_bytes, 256);
   p.choice_off = align_up(p.ticket_off + size_t(B) * 4, 256);
   p.q_off = align_up(p.choice_off + size_t(B) * L * kCand * 4, 256);
   p.ws_bytes = align_up(p.q_off + size_t(B) * L * kCand * kCand * 4, 256);
   p.M = p.MA;
   return p;
+}
+
+// One proj_tc launch over up to three problems (rows of `kind` times W^T).
+struct ProjJob {
+  int kind;
+  int M;
+  float* out;
+  const __nv_bfloat16* W;
+};
+
+static cudaError_t ensure_gemm_attr() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (!g_gemm_attr[dev & 63]) {
+    e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmem));
+    if (e != cudaSuccess) return e;
+    g_gemm_attr[dev & 63] = true;
+  }
+  return cudaSuccess;
+}
+
+static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, int kps, int d,
+                                    const __nv_bfloat16* E, const __nv_bfloat16* hidden,
+                                    const int32_t* cand_idx, const int32_t* verified, int L, int V,
+                                    float* part, cudaStream_t s, bool pdl) {
+  cudaError_t e = ensure_gemm_attr();
+  if (e != cudaSuccess) return e;
+  alignas(64) CUtensorMap tm[3];
+  GemmArgs g{};
+  int before = 0;
+  for (int i = 0; i < 3; ++i) {
+    const bool live = i < njobs;
+    const __nv_bfloat16* W = live ? jobs[i].W : jobs[0].W;
+    if (!tensor_map_bf16(W, kRank, d, kBN, &tm[i])) return cudaErrorInvalidValue;
+    g.prob[i].kind = live ? jobs[i].kind : kRowsHidden;
+    g.prob[i].M = live ? jobs[i].M : 0;
+    g.prob[i].mtiles = live ? (jobs[i].M + kBM - 1) / kBM : 0;
+    g.prob[i].out = live ? jobs[i].out : nullptr;
+    g.prob[i].part = part;
+    if (live && splits > 1) part += size_t(splits) * jobs[i].M * kRank;
+    g.tiles_before[i] = before;
+    before += g.prob[i].mtiles;
+  }
+  g.splits = splits;
+  g.kps = kps;
+  g.kblocks = d / kBK;
+  g.E = E;
+  g.hidden = hidden;
+  g.cand_idx = cand_idx;
+  g.verified = verified;
+  g.L = L;
+  g.V = V;
+  g.d = d;
+  g.err = device_error_word();
+  if (before == 0) return cudaSuccess;
+  return launch_kc(proj_tc_kernel, dim3(before * splits), dim3(kGemmThreads), kGemmSmem, s, pdl,
+                   splits, g, tm[0], tm[1], tm[2]);
 }
 
 cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
@@ -510,6 +619,8 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   qa.PA = PA;
   qa.PB = PB;
   qa.GH = GH;
+  qa.V = V;
+  qa.err = device_error_word();
   qa.cand_val = cand_val;
   qa.scores = scores;
   qa.L = p.L;
@@ -519,6 +630,58 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     qa.seeds = walk->seeds;
     qa.cycle = walk->cycle;
     qa.cand_idx = cand_idx;
+    qa.tokens = walk->tokens;
+    qa.slots = walk->slots;
+    qa.q = walk->q;
+    qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
+    qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
+    qa.qrows = reinterpret_cast<float*>(w + p.q_off);
+  }
+  return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
+}
+
+cudaError_t launch_tables_build(const __nv_bfloat16* E, const __nv_bfloat16* W_A,
+                                const __nv_bfloat16* W_B, int V, int d, float* P_A, float* P_B,
+                                cudaStream_t s) {
+  // every row of E times W_A^T and W_B^T: one launch, two problems, K unsplit
+  const ProjJob jobs[2] = {{kRowsE, V, P_A, W_A}, {kRowsE, V, P_B, W_B}};
+  return launch_proj_jobs(jobs, 2, 1, d / kBK, d, E, nullptr, nullptr, nullptr, 1, V, nullptr, s,
+                          true);
+}
+
+cudaError_t launch_gate(const SelectPlan& p, const __nv_bfloat16* hidden, const __nv_bfloat16* W_H,
+                        void* ws, cudaStream_t s, bool pdl) {
+  // the hidden rows only (GH before the sigmoid), K split over a cluster when
+  // the tiles cannot fill the GPU
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int splits, kps;
+  gate_split(p.MH, p.kblocks, splits, kps);
+  const ProjJob job{kRowsHidden, p.MH, reinterpret_cast<float*>(w + p.GH_off), W_H};
+  return launch_proj_jobs(&job, 1, splits, kps, p.d, nullptr, hidden, nullptr, nullptr, p.L, 1,
+                          reinterpret_cast<float*>(w + p.part_off), s, pdl);
+}
+
+cudaError_t launch_pair_tables(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
+                               const int32_t* verified, const float* P_A, const float* P_B, int V,
+                               float* scores, const WalkFuse* walk, void* ws, cudaStream_t s,
+                               bool pdl) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PairArgs qa{};
+  qa.tabA = P_A;
+  qa.tabB = P_B;
+  qa.verified = verified;
+  qa.V = V;
+  qa.err = device_error_word();
+  qa.GH = reinterpret_cast<float*>(w + p.GH_off);
+  qa.cand_val = cand_val;
+  qa.cand_idx = cand_idx;
+  qa.scores = scores;
+  qa.L = p.L;
+  if (walk) {
+    qa.walk = 1;
+    qa.T = walk->T;
+    qa.seeds = walk->seeds;
+    qa.cycle = walk->cycle;
     qa.tokens = walk->tokens;
     qa.slots = walk->slots;
     qa.q = walk->q;

@@ -184,6 +184,45 @@ dfl2_status dfl2_tail(const void* logits, dfl2_dtype dtype, const int32_t* verif
                       dfl2_stream stream);
 
 /* ---------------------------------------------------------------------------
+ * Precomputed token tables (a variant of the projections; the pages compute
+ * A(a) = W_A E[a] and B(b) = W_B E[b] per candidate, "DFlash 2: Keep Drafting
+ * Parallel", 方法细节 > 轻量级路径选择器, the definitions under the pair-score
+ * equation).  Both maps are linear in E[.], so P_A = E W_A^T and P_B = E W_B^T,
+ * built once per set of weights, give the same values per token (float32, the
+ * accumulation order of the GEMM aside), and the per-cycle work shrinks to
+ * gathering 1 KB rows instead of d-wide embedding rows.
+ *
+ * dfl2_tables_bytes(V): bytes of ONE table (float32 [V, 256]).
+ * dfl2_tables_build: P_A, P_B (caller-owned device memory, dfl2_tables_bytes(V)
+ *   each) from E [V, d] and W_A, W_B [256, d] (bf16, device).  d % 64 == 0.
+ *   One tcgen05 GEMM launch; rebuild whenever E, W_A or W_B change.
+ * dfl2_select_tables: as dfl2_select, with A(.) and B(.) read from the tables
+ *   (E, W_A, W_B are not needed); the gate H = sigmoid(W_H h) is still computed
+ *   per call.  Workspace: dfl2_select_workspace_size(B, L, d).
+ * dfl2_tail_tables: as dfl2_tail with the tables.  The gate projection runs on
+ *   a library-owned side stream (one per device and host thread), forked from
+ *   and joined back to `stream` with events, beside the top-16; under CUDA
+ *   graph capture the fork and join become graph edges.  Workspace:
+ *   dfl2_tail_workspace_size(B, L, V, d).
+ * Errors as for dfl2_select / dfl2_tail; a token outside [0, V) is recorded in
+ * the device error word and read as row 0.
+ * ------------------------------------------------------------------------- */
+size_t dfl2_tables_bytes(int V);
+dfl2_status dfl2_tables_build(const uint16_t* E, const uint16_t* W_A, const uint16_t* W_B, int V,
+                              int d, float* P_A, float* P_B, dfl2_stream stream);
+dfl2_status dfl2_select_tables(const int32_t* cand_idx, const float* cand_val,
+                               const int32_t* verified_tok, const uint16_t* hidden,
+                               const uint16_t* W_H, const float* P_A, const float* P_B, int B,
+                               int L, int V, int d, int r, float* scores, void* ws,
+                               size_t ws_bytes, dfl2_stream stream);
+dfl2_status dfl2_tail_tables(const void* logits, dfl2_dtype dtype, const int32_t* verified_tok,
+                             const uint16_t* hidden, const uint16_t* W_H, const float* P_A,
+                             const float* P_B, int B, int L, int V, int d, float temperature,
+                             const uint64_t* seeds, uint64_t cycle_offset, int32_t* tokens,
+                             int32_t* slots, float* q, int32_t* cand_idx, float* cand_val,
+                             float* scores, void* ws, size_t ws_bytes, dfl2_stream stream);
+
+/* ---------------------------------------------------------------------------
  * dfl2_verify: verification of the drafted block against the target's
  * distributions, the step after the walk ("DFlash 2: Keep Drafting Parallel",
  * 方法细节 > 轻量级路径选择器, "全并行打分与低延迟路径步进": lossless rejection

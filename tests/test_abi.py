@@ -31,7 +31,8 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify"):
+    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify",
+              "dfl2_tables_build", "dfl2_select_tables", "dfl2_tail_tables"):
         assert n in names
 
 
@@ -103,6 +104,28 @@ def test_verify_rejects_bad_arguments(lib):
     assert f(A, A2, None, A, A, 1, 8, 1024, 0, A, 0, A, A, None, 0, None) == INVALID   # no slots
     assert f(A, A2, A, A, A, 1, 8, 1024, 0, None, 0, A, A, None, 0, None) == INVALID   # no seeds
     assert f(A, A2, A, A + 4, A, 1, 8, 1024, 0, A, 0, A, A, None, 0, None) == INVALID  # misaligned q
+
+
+def test_tables_reject_bad_arguments(lib):
+    assert dfl2.dfl2_tables_bytes(151936) == 151936 * 256 * 4
+    assert dfl2.dfl2_tables_bytes(8) == 0
+    f = lib.dfl2_tables_build
+    assert f(A, A, A, 1024, 100, A2, A2 + 0x100000, None) == UNSUPPORTED      # d % 64
+    assert f(A, A, A, 8, 1024, A2, A2 + 0x100000, None) == INVALID             # V < 16
+    assert f(A, None, A, 1024, 1024, A2, A2 + 0x100000, None) == INVALID       # NULL W_A
+    g = lib.dfl2_select_tables
+    ws = dfl2.dfl2_select_workspace_size(1, 8, 1024)
+    assert g(A, A, A, A, A, A, A, 1, 8, 1024, 1024, 128, A2, A2, ws, None) == UNSUPPORTED  # r
+    assert g(A, A, A, A, A, None, A, 1, 8, 1024, 1024, 256, A2, A2, ws, None) == INVALID    # P_A
+    assert g(A, A, A, A, A, A, A, 1, 8, 1024, 1024, 256, A2, A2, 0, None) == WORKSPACE
+    h = lib.dfl2_tail_tables
+    tws = dfl2.dfl2_tail_workspace_size(1, 8, 1024, 1024)
+    assert h(A, 1, A, A, A, A, A, 1, 8, 1024, 1024, 1.0, None, 0, A2, None, None, None, None,
+             None, A2 + 0x100000, tws, None) == INVALID                                       # seeds
+    assert h(A, 1, A, A, A, A, A, 1, 200, 1024, 1024, 0.0, None, 0, A2, None, None, None, None,
+             None, A2 + 0x100000, tws, None) == UNSUPPORTED                                   # L
+    assert h(A, 1, A, A, A, A, A, 1, 8, 1024, 1024, 0.0, None, 0, A2, None, None, None, None,
+             None, A2 + 0x100000, 16, None) == WORKSPACE
 
 
 def test_conv_rejects_bad_arguments(lib):

@@ -47,8 +47,8 @@ def run_tail(w, lg, inp, T, seeds, cycle=0):
     return {k: v.cpu().numpy() for k, v in out.items()}
 
 
-def check_tail(w, lg, inp, T, seeds, cycle, seqs):
-    g = run_tail(w, lg, inp, T, seeds, cycle)
+def check_tail(w, lg, inp, T, seeds, cycle, seqs, runner=None):
+    g = (runner or run_tail)(w, lg, inp, T, seeds, cycle)
     V = w.V
     flat = lg.reshape(w.rows, V)
     rows = [b * w.L + t for b in seqs for t in range(w.L)]
