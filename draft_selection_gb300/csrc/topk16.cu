@@ -38,7 +38,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kTileBytes = 8192;
 constexpr int kVecPerLane = kTileBytes / 16 / 32;  // 16-byte vectors per lane per tile
-constexpr int kStages = 12;
+constexpr int kStages = 8;
 constexpr int kMaxGrid = 2048;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kCandCap = 1024;   // candidate keys buffered per row segment
@@ -52,6 +52,9 @@ constexpr size_t kSmemBytes = size_t(kStages) * kTileBytes + 2 * kStages * sizeo
                               kCand * sizeof(uint64_t) +
                               size_t(kConsumerWarps) * kCand * sizeof(float) + 32;  // flags: 5 words
 static_assert(kVecPerLane <= 32, "hit masks are 32 bits");
+static_assert((size_t(kStages) * kTileBytes + 2 * kStages * 8 + size_t(kCandCap) * 8 +
+               size_t(kConsumerWarps) * kCand * 8 + kCand * 8) % 16 == 0,
+              "the lane-maximum lists are read 16 bytes at a time");
 static_assert(kStages >= kConsumerWarps, "the held bound tiles must fit in the ring");
 
 struct TopkArgs {
@@ -343,7 +346,8 @@ __device__ __forceinline__ void rank_select16(const uint64_t* keys, int n, uint6
 
 // lm holds kConsumerWarps descending lists of 16 lane maxima.  Entry (w, i)
 // ranks as i plus, in every other list w2, the entries above it (ties go to
-// the lower list); the entry of rank 15 is the 16th largest of the union.
+// the lower list), counted with independent 16-byte loads; the entry of rank
+// 15 is the 16th largest of the union.
 __device__ __forceinline__ void rank_bound(const float* lm, float* out, int tid) {
   if (tid >= kConsumerWarps * kCand) return;
   const int w = tid / kCand;
@@ -352,22 +356,20 @@ __device__ __forceinline__ void rank_bound(const float* lm, float* out, int tid)
 #pragma unroll
   for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
     if (w2 == w) continue;
-    const float* L2 = lm + w2 * kCand;
-    int c = 0;
+    const float4* L2 = reinterpret_cast<const float4*>(lm + w2 * kCand);
+    const bool lower = w2 < w;
 #pragma unroll
-    for (int st = 16; st > 0; st >>= 1) {
-      if (c + st <= kCand) {
-        const float e = L2[c + st - 1];
-        if (e > v || (e == v && w2 < w)) c += st;
-      }
+    for (int q = 0; q < kCand / 4; ++q) {
+      const float4 e = L2[q];
+      r += (e.x > v || (lower && e.x == v)) + (e.y > v || (lower && e.y == v)) +
+           (e.z > v || (lower && e.z == v)) + (e.w > v || (lower && e.w == v));
     }
-    r += c;
   }
   if (r == kCand - 1) *out = v;
 }
 
 template <int EPV>
-__global__ void __launch_bounds__(kThreads, 2) topk16_kernel(TopkArgs a) {
+__global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + size_t(kStages) * kTileBytes);
@@ -472,8 +474,15 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_kernel(TopkArgs a) {
         tile_of(jw, tile, nvec, eb);
         lm = lane_max_tile<EPV>(tile, nvec, lane);
       }
-      lm = warp_sort32_desc_f(lm, lane);
-      if (lane < kCand) lmax[warp * kCand + lane] = lm;
+      // the lane's rank in its warp from 32 independent shuffles (ties by lane):
+      // the warp's best 16 land in lmax in descending order
+      int r = 0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float o = __shfl_sync(kFull, lm, j);
+        r += (o > lm) || (o == lm && j < lane);
+      }
+      if (r < kCand) lmax[warp * kCand + r] = lm;
     }
     if (threadIdx.x == 0) {  // both read last at the previous segment's start
       *bound_s = -INFINITY;
