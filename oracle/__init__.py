@@ -68,6 +68,8 @@ def lib():
         L.oracle_verify_uniforms.argtypes = [U64, U64, I, P]
         L.oracle_verify.argtypes = [P, P, P, P, P, I, I, I, I, P, U64, P, P]
         L.oracle_verify.restype = I
+        L.oracle_lmhead_topk.argtypes = [P, P, I, I, I, I, P, P]
+        L.oracle_lmhead_topk.restype = I
         L.oracle_round_bf16.argtypes = [D]
         L.oracle_round_bf16.restype = ctypes.c_uint16
         _lib = L
@@ -126,6 +128,26 @@ def topk(logits: np.ndarray, k: int = 16):
     if rc != 0:
         raise ValueError("oracle_topk rejected its arguments")
     shape = lg.shape[:-1] + (k,)
+    return idx.reshape(shape), val.reshape(shape)
+
+
+def lmhead_topk(hidden: np.ndarray, W_lm: np.ndarray, k: int = 16):
+    """hidden [..., d] and W_lm [V, d] as bf16 bit patterns (uint16).
+
+    Returns (idx int32 [..., k], val float64 [..., k]): the k largest exact
+    logits hidden . W_lm[v] per row, value descending then index ascending.
+    """
+    h = _c(hidden, np.uint16)
+    W = _c(W_lm, np.uint16)
+    V, d = W.shape
+    if h.shape[-1] != d:
+        raise ValueError("hidden and W_lm disagree on d")
+    R = h.size // d
+    idx = np.zeros((R, k), np.int32)
+    val = np.zeros((R, k), np.float64)
+    if lib().oracle_lmhead_topk(_ptr(h), _ptr(W), R, V, d, k, _ptr(idx), _ptr(val)) != 0:
+        raise ValueError("oracle_lmhead_topk rejected its arguments")
+    shape = h.shape[:-1] + (k,)
     return idx.reshape(shape), val.reshape(shape)
 
 

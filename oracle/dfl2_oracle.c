@@ -417,3 +417,38 @@ int oracle_verify(const float* p, const int32_t* tokens, const int32_t* slots, c
   }
   return bad ? -1 : 0;
 }
+
+/* ---------------------------------------------------------------- LM head + top-k */
+
+int oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* W_lm, int R, int V, int d, int k,
+                       int32_t* idx, double* val) {
+  if (!hidden || !W_lm || !idx || !val || R < 1 || V < k || d < 1 || k < 1) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int r = 0; r < R; ++r) {
+    double* h = (double*)malloc(sizeof(double) * (size_t)d);
+    vi_pair* all = (vi_pair*)malloc(sizeof(vi_pair) * (size_t)V);
+    if (!h || !all) {
+      bad = 1;
+      free(h);
+      free(all);
+      continue;
+    }
+    for (int c = 0; c < d; ++c) h[c] = bf16_to_double(hidden[(size_t)r * d + c]);
+    for (int v = 0; v < V; ++v) {
+      const uint16_t* w = W_lm + (size_t)v * d;
+      double acc = 0.0;
+      for (int c = 0; c < d; ++c) acc += h[c] * bf16_to_double(w[c]);
+      all[v].v = acc;
+      all[v].i = v;
+    }
+    qsort(all, (size_t)V, sizeof(vi_pair), cmp_value_desc_index_asc);
+    for (int j = 0; j < k; ++j) {
+      idx[(size_t)r * k + j] = all[j].i;
+      val[(size_t)r * k + j] = all[j].v;
+    }
+    free(h);
+    free(all);
+  }
+  return bad ? -1 : 0;
+}

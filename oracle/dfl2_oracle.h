@@ -104,6 +104,13 @@ int oracle_walk(const double* scores, const int32_t* cand_idx, int B, int L, dou
 int oracle_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
                  const uint16_t* W_c, int B, int L, int d, double* y_exact, uint16_t* y_bf16);
 
+/* Top-k of the LM head's logits [SEL "每个位置提取并保留 Top-16" applied to
+ * the drafter's LM-head output]: logits[r, v] = sum_c hidden[r, c] * W_lm[v, c]
+ * in double (bf16 inputs, exact), then the full sort of oracle_topk.  idx/val
+ * [R, k].  Returns 0, or -1 on a bad argument. */
+int oracle_lmhead_topk(const uint16_t* hidden, const uint16_t* W_lm, int R, int V, int d, int k,
+                       int32_t* idx, double* val);
+
 /* The two uniforms verification draws at block position t (reading, the pages
  * name no generator): words 0 and 1 of Philox4x32-10 with counter
  * (t, lo32(cycle), hi32(cycle), 1) and key = the sequence's seed, each
