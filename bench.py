@@ -348,6 +348,59 @@ def measure_verify(w: wl.Workload, device, steps, warmup, flush, peak_gbs):
     return res
 
 
+def measure_lmhead(w: wl.Workload, device, steps, warmup, flush, pk):
+    """LM head + top-16 from the last hidden state: the fused kernel
+    (dfl2_lmhead_topk, logits never written) against the unfused pair a
+    library user would otherwise run, a cuBLAS bf16 GEMM writing the [B*L, V]
+    logits followed by dfl2_topk over them.  Each arm in its own graph, L2
+    flushed before every replay (W_lm alone is larger than L2)."""
+    import draft_selection_gb300 as dfl2
+    inp = wl.make_lmhead_inputs(w, device, "gauss")
+    B, L, V, d = w.B, w.L, w.V, w.d
+    R = B * L
+    h, W = inp["hidden"], inp["W_lm"]
+    idx = torch.empty(B, L, 16, dtype=torch.int32, device=device)
+    val = torch.empty(B, L, 16, dtype=torch.float32, device=device)
+    ws = dfl2.workspace(dfl2.dfl2_lmhead_topk_workspace_size(B, L, V, d), device)
+    logits = torch.empty(R, V, dtype=torch.bfloat16, device=device)
+    ws_t = dfl2.workspace(dfl2.dfl2_topk_workspace_size(B, L, V), device)
+    h2 = h.view(R, d)
+    fused = lambda: dfl2.dfl2_lmhead_topk(h, W, idx, val, ws)
+    gemm = lambda: torch.matmul(h2, W.t(), out=logits)
+    unfused = lambda: (gemm(), dfl2.dfl2_topk(logits.view(B, L, V), idx, val, ws_t))
+    n = max(3, min(steps, 100))
+    res = {}
+    for name, fn in (("fused", fused), ("cublas_gemm", gemm), ("cublas_gemm_plus_topk", unfused)):
+        graph, k = capture(fn)
+        ms = summarize(time_graph(graph, n, warmup, flush))["mean_ms"]
+        res[name + "_us"] = round(ms * 1e3, 2)
+        if name == "fused":
+            res["fused_launches"] = k
+            fused_ms = ms
+    torch.cuda.synchronize()
+    assert dfl2.dfl2_device_error() == 0
+    flops = 2.0 * R * V * d
+    nbytes = V * d * 2 + R * d * 2 + R * 16 * 8
+    tflops = flops / (fused_ms * 1e-3) / 1e12
+    gbs = nbytes / (fused_ms * 1e-3) / 1e9
+    # memory-bound while the weight read outlasts the MMAs at the measured peaks
+    hbm_s = nbytes / (pk["hbm_gbs"] * 1e9)
+    tc_s = flops / (pk["bf16_tflops"] * 1e12)
+    if hbm_s >= tc_s:
+        roof = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(gbs / pk["hbm_gbs"], 4)}
+    else:
+        roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
+    res.update({"workload": w.name, "rows": R, "V": V, "d": d, "flops": flops, "bytes": nbytes,
+                "tflops": round(tflops, 1), "gbs": round(gbs, 1), "roofline": roof,
+                "speedup_vs_cublas_plus_topk": round(res["cublas_gemm_plus_topk_us"] /
+                                                     res["fused_us"], 3),
+                "inputs": "h ~ N(0,1), W_lm ~ N(0, 1/sqrt(d)), bf16"})
+    del inp, logits
+    return res
+
+
 def measure_e2e(case: Case, g_step, steps, warmup, flush):
     """The same step with the inputs copied from pinned host memory and the
     result read back inside the timed region."""
@@ -482,13 +535,25 @@ def profile_op(args) -> int:
     build.build()
     import draft_selection_gb300 as dfl2
     torch.cuda.set_device(0)
-    case = Case(wl.WORKLOADS[args.workload], 1.0, torch.device("cuda", 0))
+    dev = torch.device("cuda", 0)
+    if args.profile_op == "lmhead":
+        w = wl.WORKLOADS[args.workload]
+        lm = wl.make_lmhead_inputs(w, dev, "gauss")
+        lm_idx = torch.empty(w.B, w.L, 16, dtype=torch.int32, device=dev)
+        lm_val = torch.empty(w.B, w.L, 16, dtype=torch.float32, device=dev)
+        lm_ws = dfl2.workspace(dfl2.dfl2_lmhead_topk_workspace_size(w.B, w.L, w.V, w.d), dev)
+        case = None
+    else:
+        case = Case(wl.WORKLOADS[args.workload], 1.0, dev)
     if args.profile_op in ("select", "walk"):
         case.topk()
     if args.profile_op == "walk":
         case.select()
-    fn = {"topk": case.topk, "select": case.select, "walk": case.walk,
-          "conv": lambda: case.conv(0), "tail": case.tail, "step": case.step}[args.profile_op]
+    if case is None:
+        fn = lambda: dfl2.dfl2_lmhead_topk(lm["hidden"], lm["W_lm"], lm_idx, lm_val, lm_ws)
+    else:
+        fn = {"topk": case.topk, "select": case.select, "walk": case.walk,
+              "conv": lambda: case.conv(0), "tail": case.tail, "step": case.step}[args.profile_op]
     for _ in range(args.steps):
         fn()
     torch.cuda.synchronize()
@@ -508,7 +573,8 @@ def main():
     ap.add_argument("--batched", default=BATCHED, help="second workload ('' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
-    ap.add_argument("--profile-op", choices=["topk", "select", "walk", "conv", "tail", "step"],
+    ap.add_argument("--profile-op",
+                    choices=["topk", "select", "walk", "conv", "tail", "step", "lmhead"],
                     help="run one op --steps times, untimed, for a profiler; no JSON line")
     args = ap.parse_args()
     if args.profile_op:
@@ -566,6 +632,11 @@ def main():
         }
         del cb
         verify[wb.name] = measure_verify(wb, device, args.steps, args.warmup, flush, pk["hbm_gbs"])
+    lmhead = {}
+    for name in (w.name, args.batched):
+        if name:
+            lmhead[name] = measure_lmhead(wl.WORKLOADS[name], device, args.steps, args.warmup,
+                                          flush, pk)
     clk = clocks.stop()
 
     cpu = None
@@ -591,6 +662,7 @@ def main():
             "tables": res["tables"],
             "b64": batched,
             "verify": verify,
+            "lmhead_topk": lmhead,
             "e2e": {"value": round(e2e_ms * 1e3 / world, 2), "unit": "µs per draft block",
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": res["kernels_per_step"] * args.steps,

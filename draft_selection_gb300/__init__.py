@@ -56,6 +56,9 @@ def load():
     L.dfl2_topk.argtypes = [P, I, I, I, I, I, P, P, P, SZ, P]
     L.dfl2_topk_noalloc.argtypes = [P, I, I, I, I, I, P, P, P]
     L.dfl2_topk_noalloc.restype = I
+    L.dfl2_lmhead_topk_workspace_size.argtypes = [I, I, I, I]
+    L.dfl2_lmhead_topk_workspace_size.restype = SZ
+    L.dfl2_lmhead_topk.argtypes = [P, P, I, I, I, I, I, P, P, P, SZ, P]
     L.dfl2_select_workspace_size.argtypes = [I, I, I]
     L.dfl2_select_workspace_size.restype = SZ
     L.dfl2_select.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]
@@ -143,6 +146,10 @@ def dfl2_topk_workspace_size(B: int, L: int, V: int) -> int:
     return int(load().dfl2_topk_workspace_size(B, L, V))
 
 
+def dfl2_lmhead_topk_workspace_size(B: int, L: int, V: int, d: int) -> int:
+    return int(load().dfl2_lmhead_topk_workspace_size(B, L, V, d))
+
+
 def dfl2_select_workspace_size(B: int, L: int, d: int) -> int:
     return int(load().dfl2_select_workspace_size(B, L, d))
 
@@ -169,6 +176,20 @@ def dfl2_topk(logits, cand_idx, cand_val, ws, k: int = NCAND, stream=None, *, di
     wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
     _check(load().dfl2_topk(_ptr(logits), dt, B, L, V, k, _ptr(cand_idx), _ptr(cand_val),
                             _ptr(ws), wb, _stream(stream)))
+
+
+def dfl2_lmhead_topk(hidden, W_lm, cand_idx, cand_val, ws, k: int = NCAND, stream=None, *,
+                     dims=None, ws_bytes=None) -> None:
+    """hidden bf16 [B,L,d], W_lm bf16 [V,d] -> the top 16 of hidden . W_lm^T per row:
+    cand_idx int32 [B,L,16], cand_val float32 [B,L,16]."""
+    if dims is not None:
+        B, L, V, d = dims
+    else:
+        B, L, d = hidden.shape
+        V = W_lm.shape[0]
+    wb = ws_bytes if ws_bytes is not None else _nbytes(ws)
+    _check(load().dfl2_lmhead_topk(_ptr(hidden), _ptr(W_lm), B, L, V, d, k, _ptr(cand_idx),
+                                   _ptr(cand_val), _ptr(ws), wb, _stream(stream)))
 
 
 def dfl2_topk_noalloc(logits, cand_idx, cand_val, k: int = NCAND, stream=None, *, dims=None,

@@ -290,6 +290,33 @@ dfl2_status dfl2_topk(const void* logits, dfl2_dtype dtype, int B, int L, int V,
   return DFL2_OK;
 }
 
+size_t dfl2_lmhead_topk_workspace_size(int B, int L, int V, int d) {
+  if (B < 1 || L < 1 || V < dfl2::kCand || d < 1) return 0;
+  return dfl2::lmhead_plan(B * L, V, d).ws_bytes;
+}
+
+dfl2_status dfl2_lmhead_topk(const uint16_t* hidden, const uint16_t* W_lm, int B, int L, int V,
+                             int d, int k, int32_t* cand_idx, float* cand_val, void* ws,
+                             size_t ws_bytes, dfl2_stream stream) {
+  DFL2_TRY(check_shape(B, L));
+  if (k != dfl2::kCand) return fail(DFL2_ERR_UNSUPPORTED, "k=%d: only 16 candidates", k);
+  if (V < dfl2::kCand) return fail(DFL2_ERR_INVALID_ARG, "V=%d < 16", V);
+  if (d < 8 || d % 8 != 0)
+    return fail(DFL2_ERR_UNSUPPORTED, "d=%d: rows of hidden and W_lm must be 16-byte multiples", d);
+  const dfl2::LmheadPlan plan = dfl2::lmhead_plan(B * L, V, d);
+  const Ptrs ptrs = {{hidden, "hidden"}, {W_lm, "W_lm"}, {cand_idx, "cand_idx"},
+                     {cand_val, "cand_val"}};
+  DFL2_TRY(check_host(ptrs));
+  DFL2_TRY(check_ws(ws, ws_bytes, plan.ws_bytes));
+  DFL2_TRY(ensure_device());
+  DFL2_TRY(check_device(ptrs));
+  DFL2_TRY(check_device_ptr(ws, "workspace"));
+  cudaError_t e = dfl2::launch_lmhead_topk(plan, bf(hidden), bf(W_lm), cand_idx, cand_val, ws,
+                                           reinterpret_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "LM head + top-16 launch");
+  return DFL2_OK;
+}
+
 size_t dfl2_select_workspace_size(int B, int L, int d) {
   if (B < 1 || L < 1 || d < 1) return 0;
   return dfl2::select_plan(B, L, d).ws_bytes;

@@ -250,6 +250,21 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
                          const __nv_bfloat16* W_c, int B, int L, int d, __nv_bfloat16* y,
                          cudaStream_t s);
 
+// ---- LM head + top-16 (lmhead.cu) ---------------------------------------------
+struct LmheadPlan {
+  int R, V, d;
+  int rtiles;          // ceil(R / 128)
+  int ntiles;          // ceil(V / 256)
+  int kblocks;         // ceil(d / 64)
+  int max_splits;      // CTAs per row tile the workspace has room for
+  size_t lists_off;    // uint64 [R][splits][16] partial lists, one per row and CTA
+  size_t ws_bytes;
+};
+LmheadPlan lmhead_plan(int R, int V, int d);
+cudaError_t launch_lmhead_topk(const LmheadPlan& p, const __nv_bfloat16* hidden,
+                               const __nv_bfloat16* W_lm, int32_t* idx, float* val, void* ws,
+                               cudaStream_t s, bool pdl);
+
 // ---- helpers ------------------------------------------------------------------
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 

@@ -175,6 +175,45 @@ def make_verify_inputs(w: Workload, device="cpu", temperature: float = 1.0,
             "seeds": philox_seeds(w, salt=7)}
 
 
+def make_lmhead_inputs(w: Workload, device="cpu", kind: str = "gauss") -> dict:
+    """Synthetic inputs for the LM head + top-16: the drafter's last hidden
+    state [B, L, d] and an LM-head weight W_lm [V, d], both bf16.
+
+    kind "gauss": h ~ N(0, 1), W_lm ~ N(0, 1/sqrt(d)), so the logits are about
+    N(0, 1).  kind "int": h and W_lm uniform integers in [-3, 3]; every partial
+    sum is an integer below 2^24, so float32 accumulation is exact in any order
+    and the result can be compared bit for bit.  kind "ties": W_lm as in "int",
+    h one-hot on 4 random channels, so the logits take 25 values and the top 16
+    is decided by the index tie rule.  W_lm is drawn in row chunks to bound the
+    temporaries."""
+    B, L, V, d = w.B, w.L, w.V, w.d
+    g = _generator(w, f"lmhead.{kind}.hidden", device)
+    if kind == "gauss":
+        hidden = torch.randn(B, L, d, generator=g, device=device).to(torch.bfloat16)
+    elif kind == "int":
+        hidden = torch.randint(-3, 4, (B, L, d), generator=g, device=device,
+                               dtype=torch.int8).to(torch.bfloat16)
+    elif kind == "ties":
+        hidden = torch.zeros(B * L, d, dtype=torch.bfloat16, device=device)
+        ch = torch.stack([torch.randperm(d, generator=g, device=device)[:4]
+                          for _ in range(B * L)])
+        hidden.scatter_(1, ch, torch.ones(B * L, 4, dtype=torch.bfloat16, device=device))
+        hidden = hidden.view(B, L, d)
+    else:
+        raise ValueError(f"unknown LM-head input kind {kind!r}")
+    g = _generator(w, f"lmhead.{kind}.W", device)
+    W = torch.empty(V, d, dtype=torch.bfloat16, device=device)
+    chunk = max(1, (1 << 26) // d)
+    for r0 in range(0, V, chunk):
+        n = min(chunk, V - r0)
+        if kind == "gauss":
+            W[r0:r0 + n] = (torch.randn(n, d, generator=g, device=device) / d ** 0.5).to(torch.bfloat16)
+        else:
+            W[r0:r0 + n] = torch.randint(-3, 4, (n, d), generator=g, device=device,
+                                         dtype=torch.int8).to(torch.bfloat16)
+    return {"hidden": hidden.contiguous(), "W_lm": W}
+
+
 def bf16_bits(t: torch.Tensor) -> np.ndarray:
     """A bf16 tensor's bit patterns as a host uint16 array (what the oracle takes)."""
     assert t.dtype == torch.bfloat16

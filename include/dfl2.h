@@ -102,6 +102,34 @@ dfl2_status dfl2_topk(const void* logits, dfl2_dtype dtype, int B, int L, int V,
                       int32_t* cand_idx, float* cand_val, void* ws, size_t ws_bytes,
                       dfl2_stream stream);
 
+/* ------------------------------------------------------------------ LM head + top-16
+ * The logits the top-16 step reads are the drafter's LM head applied to its
+ * last hidden state ("DFlash 2: Keep Drafting Parallel", 方法细节 >
+ * 轻量级路径选择器: U_t(.) is the drafter's own logit at position t).  This
+ * entry point computes U_t(v) = sum_c hidden[t, c] * W_lm[v, c] (bf16 inputs,
+ * float32 accumulation on the tensor cores) and keeps only the 16 largest per
+ * row, inside the GEMM's epilogue: the [B*L, V] logits are never written.
+ *   hidden  bf16 [B, L, d] row-major, device, 16-byte aligned.
+ *   W_lm    bf16 [V, d] row-major, device, 16-byte aligned (a tied embedding
+ *           table E may be passed).
+ *   d       a multiple of 8 (16-byte rows); any V >= 16, any B*L >= 1.
+ *   k       must be 16.
+ *   Writes cand_idx int32 [B,L,16] and cand_val float32 [B,L,16] in the order
+ *   of dfl2_topk (value descending, index ascending).  cand_val is the float32
+ *   accumulator, so rows whose 16th and 17th logits differ by less than the
+ *   accumulation error may pick either; with inputs whose partial sums are
+ *   exact in float32 (e.g. small integers) the result equals dfl2_topk on the
+ *   exact logits.  NaN/Inf inputs are not supported.
+ *   ws: dfl2_lmhead_topk_workspace_size bytes (partial lists, not needing
+ *   initialisation).  Two kernel launches on `stream`.
+ * Errors: DFL2_ERR_INVALID_ARG (NULL/unaligned/host pointers, V < 16, B or L
+ * < 1), DFL2_ERR_UNSUPPORTED (k != 16, d % 8 != 0), DFL2_ERR_WORKSPACE.
+ */
+size_t dfl2_lmhead_topk_workspace_size(int B, int L, int V, int d);
+dfl2_status dfl2_lmhead_topk(const uint16_t* hidden, const uint16_t* W_lm, int B, int L, int V,
+                             int d, int k, int32_t* cand_idx, float* cand_val, void* ws,
+                             size_t ws_bytes, dfl2_stream stream);
+
 /* ------------------------------------------------------------------ top-16, no allocation
  * No counterpart on the pages: a convenience of this library.  The same result
  * as dfl2_topk, for callers that cannot allocate device memory, such as serving

@@ -32,7 +32,7 @@ def lib():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify",
-              "dfl2_tables_build", "dfl2_select_tables", "dfl2_tail_tables"):
+              "dfl2_tables_build", "dfl2_select_tables", "dfl2_tail_tables", "dfl2_lmhead_topk"):
         assert n in names
 
 
@@ -62,6 +62,21 @@ def test_topk_rejects_bad_arguments(lib):
     assert f(A, 1, 1, 8, 1024, 16, A, A, None, ws, None) == WORKSPACE     # no workspace
     assert f(A, 1, 1, 8, 1024, 16, A, A, A, ws - 1, None) == WORKSPACE    # too small
     assert "workspace" in dfl2.dfl2_last_error()
+
+
+def test_lmhead_topk_rejects_bad_arguments(lib):
+    ws = dfl2.dfl2_lmhead_topk_workspace_size(1, 16, 151936, 2560)
+    assert ws > 0
+    assert dfl2.dfl2_lmhead_topk_workspace_size(0, 16, 151936, 2560) == 0
+    f = lib.dfl2_lmhead_topk
+    assert f(A, A2, 1, 16, 151936, 2560, 17, A, A, A, ws, None) == UNSUPPORTED   # k != 16
+    assert f(A, A2, 1, 16, 151936, 2564, 16, A, A, A, ws, None) == UNSUPPORTED   # d % 8
+    assert f(A, A2, 1, 16, 15, 2560, 16, A, A, A, ws, None) == INVALID           # V < 16
+    assert f(A, A2, 0, 16, 151936, 2560, 16, A, A, A, ws, None) == INVALID       # B = 0
+    assert f(None, A2, 1, 16, 151936, 2560, 16, A, A, A, ws, None) == INVALID    # NULL hidden
+    assert f(A, A2 + 8, 1, 16, 151936, 2560, 16, A, A, A, ws, None) == INVALID   # unaligned W_lm
+    assert f(A, A2, 1, 16, 151936, 2560, 16, A, A, None, ws, None) == WORKSPACE  # no workspace
+    assert f(A, A2, 1, 16, 151936, 2560, 16, A, A, A, ws - 1, None) == WORKSPACE
 
 
 def test_select_rejects_bad_arguments(lib):
