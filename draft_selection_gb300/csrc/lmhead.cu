@@ -41,18 +41,26 @@ namespace {
 constexpr int kLBM = 128;                  // hidden rows per tile (TMEM lanes)
 constexpr int kLBN = 256;                  // vocabulary entries per tile (fp32 columns)
 constexpr int kLBK = 64;                   // K per stage: one 128-byte swizzle row of bf16
-constexpr int kLStages = 4;
+constexpr int kLMaxStages = 5;
 constexpr int kLEpiWarps = 8;              // two per TMEM lane quarter
 constexpr int kLThreads = (2 + kLEpiWarps) * 32;
 constexpr int kLHalf = kLBN / 2;           // columns per epilogue warp per tile
 constexpr int kLAStage = kLBM * kLBK * 2;  // 16 KB
 constexpr int kLBStage = kLBN * kLBK * 2;  // 32 KB
 constexpr uint32_t kLTmemCols = 2 * kLBN;  // two accumulators
-constexpr size_t kLBarBytes = (4 * kLStages + 8) * sizeof(uint64_t);
+constexpr size_t kLBarBytes = (2 * kLMaxStages + 8) * sizeof(uint64_t);
 constexpr size_t kLThrBytes = 2 * kLBM * sizeof(float);           // per half, per row
 constexpr size_t kLPairBytes = size_t(kLBM) * kCand * sizeof(uint64_t);  // half 1's lists
-constexpr size_t kLSmemBytes =
-    1024 + size_t(kLStages) * (kLAStage + kLBStage) + kLBarBytes + kLThrBytes + kLPairBytes;
+constexpr size_t kLFixedBytes = 1024 + kLBarBytes + kLThrBytes + kLPairBytes;
+constexpr size_t kLSmemMax = 232448;  // the opt-in shared memory of one CTA
+// Stage s holds the h tile (a_rows rows, rounded up to a 1024-byte swizzle
+// atom) and then the W_lm tile.  The MMA reads 128 rows of h from the stage's
+// start; with fewer rows loaded the rest falls inside the same stage (over the
+// W_lm tile) and only feeds accumulator rows past R, which nobody reads.
+__host__ __device__ constexpr int lm_a_bytes(int a_rows) { return (a_rows * 128 + 1023) / 1024 * 1024; }
+__host__ __device__ constexpr int lm_stage_bytes(int a_rows) { return lm_a_bytes(a_rows) + kLBStage; }
+static_assert(lm_stage_bytes(8) >= kLAStage, "the MMA's 128-row read of h stays in its stage");
+static_assert(kLFixedBytes + 4 * size_t(lm_stage_bytes(128)) <= kLSmemMax, "four full stages fit");
 constexpr int kLMaxSplits = 256;           // CTAs per row tile (workspace bound)
 constexpr unsigned kAll = 0xffffffffu;
 
@@ -62,15 +70,11 @@ struct LmArgs {
   int ntiles;       // ceil(V / 256)
   int kblocks;      // ceil(d / 64); K past d reads zeros
   int a_rows;       // rows of the hidden box: R rounded up to 8, at most 128
+  int stages;       // pipeline stages: 4 or 5 (more measured slower at B*L = 16)
   uint64_t* lists;  // [R][vsplits][16] descending keys (0 = empty)
   uint32_t* err;
 };
 
-__device__ __forceinline__ uint64_t lm_shfl_xor64(uint64_t v, int m) {
-  const uint32_t lo = __shfl_xor_sync(kAll, static_cast<uint32_t>(v), m);
-  const uint32_t hi = __shfl_xor_sync(kAll, static_cast<uint32_t>(v >> 32), m);
-  return (static_cast<uint64_t>(hi) << 32) | lo;
-}
 __device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -163,11 +167,12 @@ __global__ void __launch_bounds__(kLThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* sA = smem;                                // [stages][128 rows][128 B]
-  uint8_t* sB = smem + size_t(kLStages) * kLAStage;  // [stages][256 rows][128 B]
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(sB + size_t(kLStages) * kLBStage);
-  uint64_t* empty_bar = full_bar + kLStages;
-  uint64_t* accf_bar = empty_bar + kLStages;  // [2] accumulator b complete
+  const int nst = a.stages;
+  const int sbytes = lm_stage_bytes(a.a_rows), abytes = lm_a_bytes(a.a_rows);
+  uint8_t* stage0 = smem;  // [stages][h rows | 256 W_lm rows][128 B]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + size_t(nst) * sbytes);
+  uint64_t* empty_bar = full_bar + kLMaxStages;
+  uint64_t* accf_bar = empty_bar + kLMaxStages;  // [2] accumulator b complete
   uint64_t* acce_bar = accf_bar + 2;          // [2] accumulator b read out
   uint64_t* done_bar = acce_bar + 2;          // the MMA issuer's last commit
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done_bar + 1);
@@ -182,7 +187,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
   const int nt = t_hi - t_lo;  // >= 1: vsplits <= ntiles
 
   if (tid == 0) {
-    for (int s = 0; s < kLStages; ++s) {
+    for (int s = 0; s < nst; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -216,24 +221,25 @@ __global__ void __launch_bounds__(kLThreads, 1)
       for (int i = 0; i < nt && ok; ++i) {
         const int n0 = (t_lo + i) * kLBN;
         for (int kb = 0; kb < a.kblocks; ++kb, ++it) {
-          if (it >= kLStages && !mbar_wait(&empty_bar[s], ph ^ 1)) {
+          if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1)) {
             record_error(a.err, kDevErrGemm);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full_bar[s], tx);
-          tma_load_2d(sA + size_t(s) * kLAStage, &tmH, kb * kLBK, m0, &full_bar[s]);
-          tma_load_2d(sB + size_t(s) * kLBStage, &tmW, kb * kLBK, n0, &full_bar[s]);
-          if (++s == kLStages) {
+          uint8_t* st = stage0 + size_t(s) * sbytes;
+          tma_load_2d(st, &tmH, kb * kLBK, m0, &full_bar[s]);
+          tma_load_2d(st + abytes, &tmW, kb * kLBK, n0, &full_bar[s]);
+          if (++s == nst) {
             s = 0;
             ph ^= 1;
           }
         }
       }
-      // the last (up to kLStages) copies issued: their phases complete when they land
-      for (int back = 1; back <= kLStages && back <= it; ++back) {
+      // the last (up to nst) copies issued: their phases complete when they land
+      for (int back = 1; back <= nst && back <= it; ++back) {
         const int j = it - back;
-        mbar_wait(&full_bar[j % kLStages], (j / kLStages) & 1);
+        mbar_wait(&full_bar[j % nst], (j / nst) & 1);
       }
     }
     __syncwarp();
@@ -257,13 +263,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kLAStage);
-          const uint64_t bd = umma_desc_sw128(sB + size_t(s) * kLBStage);
+          const uint8_t* st = stage0 + size_t(s) * sbytes;
+          const uint64_t ad = umma_desc_sw128(st);
+          const uint64_t bd = umma_desc_sw128(st + abytes);
 #pragma unroll
           for (int k = 0; k < kLBK / 16; ++k)
             umma_bf16(acc, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           umma_commit(&empty_bar[s]);
-          if (++s == kLStages) {
+          if (++s == nst) {
             s = 0;
             ph ^= 1;
           }
@@ -381,12 +388,12 @@ __device__ __forceinline__ uint64_t warp_top16_of_lists(uint64_t (&k)[kCand], in
   uint64_t out = 0ull;
 #pragma unroll 1
   for (int r = 0; r < kCand; ++r) {
-    uint64_t m = k[0];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const uint64_t y = lm_shfl_xor64(m, o);
-      m = y > m ? y : m;
-    }
+    // the warp's largest head: the largest high word, then the largest low
+    // word among the lanes holding it (one reduction instruction each)
+    const uint32_t hi = static_cast<uint32_t>(k[0] >> 32), lo = static_cast<uint32_t>(k[0]);
+    const uint32_t mh = __reduce_max_sync(kAll, hi);
+    const uint32_t ml = __reduce_max_sync(kAll, hi == mh ? lo : 0u);
+    const uint64_t m = (static_cast<uint64_t>(mh) << 32) | ml;
     if (lane == r) out = m;
     if (m != 0ull && k[0] == m) {  // keys are unique: one lane pops
 #pragma unroll
@@ -472,7 +479,7 @@ cudaError_t launch_lmhead_topk(const LmheadPlan& p, const __nv_bfloat16* hidden,
   if (e != cudaSuccess) return e;
   if (!g_lm_attr[dev & 63]) {
     e = cudaFuncSetAttribute(lmhead_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kLSmemBytes));
+                             static_cast<int>(kLSmemMax));
     if (e != cudaSuccess) return e;
     g_lm_attr[dev & 63] = true;
   }
@@ -485,13 +492,16 @@ cudaError_t launch_lmhead_topk(const LmheadPlan& p, const __nv_bfloat16* hidden,
   a.kblocks = p.kblocks;
   a.vsplits = std::max(1, std::min(p.max_splits, sms / p.rtiles));
   a.a_rows = p.R >= kLBM ? kLBM : (p.R + 7) / 8 * 8;
+  const size_t sbytes = lm_stage_bytes(a.a_rows);
+  a.stages = static_cast<int>(std::min<size_t>(kLMaxStages, (kLSmemMax - kLFixedBytes) / sbytes));
+  const size_t smem = kLFixedBytes + size_t(a.stages) * sbytes;
   a.lists = reinterpret_cast<uint64_t*>(static_cast<uint8_t*>(ws) + p.lists_off);
   a.err = device_error_word();
   alignas(64) CUtensorMap tmH, tmW;
   if (!tensor_map_bf16(hidden, uint64_t(p.R), uint64_t(p.d), static_cast<uint32_t>(a.a_rows), &tmH) ||
       !tensor_map_bf16(W_lm, uint64_t(p.V), uint64_t(p.d), kLBN, &tmW))
     return cudaErrorInvalidValue;
-  e = launch_k(lmhead_topk_kernel, dim3(a.vsplits, p.rtiles), dim3(kLThreads), kLSmemBytes, s, pdl,
+  e = launch_k(lmhead_topk_kernel, dim3(a.vsplits, p.rtiles), dim3(kLThreads), smem, s, pdl,
                a, tmH, tmW);
   if (e != cudaSuccess) return e;
   const int nl = a.vsplits;
