@@ -40,9 +40,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # entry is removed when its kernel changes; ops without one report null.
 NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
-    ("topk", "serving_b64"): 314978816,     # topk16_kernel_serving_b64.md
+    ("topk", "serving_b64"): 314433792,     # topk16_kernel_serving_b64.md
     ("conv", "drafter4b_l16"): 1785088,     # conv_small_drafter4b_l16.md
     ("conv", "serving_b64"): 7277056,       # conv_tc_serving_b64.md
+    ("lmhead", "drafter4b_l16"): 781673728,  # lmhead_topk_kernel_drafter4b_l16.md
+    ("lmhead", "serving_b64"): 786832384,    # lmhead_topk_kernel_serving_b64.md
 }
 
 
@@ -392,6 +394,7 @@ def measure_lmhead(w: wl.Workload, device, steps, warmup, flush, pk):
     else:
         roof = {"bound": "tensor", "achieved": round(tflops, 1), "peak": pk["bf16_tflops"],
                 "unit": "TFLOP/s", "frac": round(tflops / pk["bf16_tflops"], 4)}
+    roof["traffic"] = NCU_TRAFFIC.get(("lmhead", w.name))
     res.update({"workload": w.name, "rows": R, "V": V, "d": d, "flops": flops, "bytes": nbytes,
                 "tflops": round(tflops, 1), "gbs": round(gbs, 1), "roofline": roof,
                 "speedup_vs_cublas_plus_topk": round(res["cublas_gemm_plus_topk_us"] /
