@@ -14,7 +14,9 @@
 // K is split over a thread-block cluster and the partial corrections are summed
 // through distributed shared memory, each CTA then mixing its slice of rows.
 //
-// For few positions (R <= 64, batch 1) a transposed kernel computes
+// For at most 16 positions (batch 1) a CUDA-core GEMV kernel spreads the
+// groups over the whole GPU, one group mixed per CTA (conv_gemv_kernel).
+// For 17..64 positions a transposed kernel computes
 // corr^T = W_sel x^T instead: the 128 W_c rows of 64 groups (both taps) are the
 // A operand, loaded by TMA with no padding, and the R positions are N.  K is
 // split over a cluster; each CTA pushes its small partial (128 x R) to the CTA
@@ -484,6 +486,273 @@ __global__ void __launch_bounds__(kCThreads, 1)
 
 bool g_conv_small_attr[64];
 
+// ============================================================================
+// At most 16 positions (batch 1): one correction group mixed per CTA.
+// ============================================================================
+// A cluster of C CTAs owns C consecutive correction groups.  CTA `rank` copies
+// the K slice [rank*d/C, (rank+1)*d/C) of the cluster's 2C W_c rows and of
+// every position of x into shared memory (bulk copies, in two K halves with a
+// barrier each, so half the warps start on the first half while the second
+// lands), forms the R x 2C partial corrections with warp-level bf16 MMAs
+// (m16n8k16: the positions are M, the W_c rows N, float32 accumulators; each
+// warp a share of the K steps), adds the warps' partials and sends each
+// group's two rows to the CTA that mixes the group with st.async, which
+// counts the bytes on the receiver's mbarrier: no cluster-wide barrier at the
+// end.  The receiver sums the C slices in rank order and applies the 2-tap mix
+// to its 16 channels.  The contraction is 2 x R x d per group, far below a
+// tcgen05 tile (M >= 64), and the call is latency-bound, so the warp-level MMA
+// is the cheaper instrument here.
+// The kernel lets the next launch on the stream start at once and, before
+// waiting on the previous launch, prefetches its slices of W_c and x into L2 (a
+// prefetch into L2 is coherent with writes still in flight, so nothing stale is
+// read); every real read follows the dependency wait.
+constexpr int kGvThreads = 256;  // 8 warps
+constexpr int kGvMaxR = 16;      // positions = the MMA's 16 rows
+constexpr size_t kGvSmemMax = 200 * 1024;
+
+struct ConvGemvArgs {
+  const __nv_bfloat16* x;       // [R, d]
+  const __nv_bfloat16* x_prev;  // [B, d]
+  const float* base;            // [2, d]
+  const __nv_bfloat16* W_c;     // [2G, d]
+  __nv_bfloat16* y;             // [R, d]
+  int R, L, d, G;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr int gemv_pitch(int d, int C) { return 2 * (d / C) + 16; }
+__host__ __device__ constexpr size_t gemv_smem_bytes(int d, int C) {
+  // [16 x rows | 2C W_c rows] (padded pitch) [warp partials 8 x 16 x 8 f32]
+  // [receive C x 2 x 16 f32] [3 mbarriers]
+  return size_t(16 + 2 * C) * gemv_pitch(d, C) + 8 * 16 * 8 * 4 + size_t(C) * 2 * 16 * 4 + 32;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t r[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816_bf16(float d[4], const uint32_t a[4], const uint32_t b[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// 4-byte store into CTA `rank`'s shared memory, counted as transaction bytes on
+// that CTA's mbarrier at the same offset as `bar`.
+__device__ __forceinline__ void st_async_f32(const void* local, uint32_t rank, float v,
+                                             const uint64_t* bar) {
+  const uint32_t a = dsmem_addr(local, rank), b = dsmem_addr(bar, rank);
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(a),
+               "f"(v), "r"(b)
+               : "memory");
+}
+__device__ __forceinline__ void bf8_to_f32(const uint4 v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
+}
+
+template <int C>
+__global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArgs a) {
+  constexpr int NR = 2 * C;  // W_c rows of the cluster, tap-major: row r = tap r/C, group r%C
+  static_assert(NR <= 8, "the W_c rows are the MMA's 8 columns");
+  extern __shared__ __align__(128) uint8_t gsm[];
+  const int d = a.d, ks = d / C, pitch = gemv_pitch(d, C);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int gc0 = (blockIdx.x / C) * C;  // first group of the cluster
+  const int gmix = gc0 + rank;           // the group this CTA mixes
+  const int k0 = rank * ks;
+  uint8_t* xs = gsm;                                // [16][pitch]
+  uint8_t* wsm = gsm + size_t(16) * pitch;          // [NR][pitch]
+  float* red = reinterpret_cast<float*>(wsm + size_t(NR) * pitch);  // [8][16][8]
+  float* recv = red + 8 * 16 * 8;                   // [C][2][16]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(recv + C * 2 * 16);  // [0..1] K halves, [2] receive
+  // K halves: two stages when each half is a whole number of 16-wide steps
+  const int nst = (ks / 2) % 16 == 0 ? 2 : 1;
+  const int hk = ks / nst;  // elements per stage
+
+  pdl_launch_dependents();
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    mbar_init(&bar[2], 1);
+    fence_mbar_init();
+    // every CTA of the cluster (this one included) sends 2 x R floats here
+    if (C > 1) mbar_arrive_expect_tx(&bar[2], uint32_t(C) * 2u * uint32_t(a.R) * 4u);
+  }
+  if (tid < NR) {
+    const int g = gc0 + tid % C;
+    if (g < a.G) prefetch_l2(a.W_c + (size_t(tid / C) * a.G + g) * d + k0, uint32_t(ks) * 2u);
+  } else if (tid >= 32 && tid < 32 + a.R) {
+    prefetch_l2(a.x + size_t(tid - 32) * d + k0, uint32_t(ks) * 2u);
+  }
+  if constexpr (C > 1) cluster_arrive_release();  // barrier inits visible to the peers
+  __syncthreads();
+  pdl_wait();
+
+  if (warp == 0) {
+    // lane i < R: x row i; lane 16 + r: W_c row r (both K halves, one barrier each)
+    if (lane == 0) {
+      int nw = 0;
+      for (int r = 0; r < NR; ++r) nw += gc0 + r % C < a.G;
+      for (int s = 0; s < nst; ++s)
+        mbar_arrive_expect_tx(&bar[s], uint32_t(a.R + nw) * uint32_t(hk) * 2u);
+    }
+    __syncwarp();
+    const __nv_bfloat16* src = nullptr;
+    uint8_t* dst = nullptr;
+    if (lane < a.R) {
+      src = a.x + size_t(lane) * d + k0;
+      dst = xs + size_t(lane) * pitch;
+    } else if (lane >= 16 && lane < 16 + NR && gc0 + (lane - 16) % C < a.G) {
+      const int r = lane - 16;
+      src = a.W_c + (size_t(r / C) * a.G + gc0 + r % C) * d + k0;
+      dst = wsm + size_t(r) * pitch;
+    }
+    if (src)
+      for (int s = 0; s < nst; ++s)
+        bulk_g2s(dst + size_t(s) * hk * 2, src + size_t(s) * hk, uint32_t(hk) * 2u, &bar[s]);
+  }
+  // ---- operands of the mix (one thread per position and half group), in flight early ----
+  const bool mixer = tid < 2 * a.R && gmix < a.G;
+  uint4 xt = make_uint4(0u, 0u, 0u, 0u), xm = xt;
+  float4 b0[2], b1[2];
+  if (mixer) {
+    const int p = tid >> 1, c = 16 * gmix + 8 * (tid & 1);
+    const int t = p % a.L;
+    xt = __ldcg(reinterpret_cast<const uint4*>(a.x + size_t(p) * d + c));
+    xm = __ldcg(reinterpret_cast<const uint4*>(
+        (t > 0 ? a.x + size_t(p - 1) * d : a.x_prev + size_t(p / a.L) * d) + c));
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      b0[h] = __ldcg(reinterpret_cast<const float4*>(a.base + c) + h);
+      b1[h] = __ldcg(reinterpret_cast<const float4*>(a.base + d + c) + h);
+    }
+  }
+  // ---- partial corrections: acc = x_slice (16 x K) * W_slice^T (K x 8) over this warp's steps ----
+  {
+    const int st = nst == 2 ? warp >> 2 : 0;       // the K half this warp reads
+    const int wi = nst == 2 ? warp & 3 : warp;     // its index among that half's warps
+    const int nw = nst == 2 ? 4 : 8;
+    const int steps = hk / 16;
+    const int s0 = st * steps + wi * steps / nw, s1 = st * steps + (wi + 1) * steps / nw;
+    const int arow = lane & 15, acol = (lane >> 4) * 8;
+    const int rb = lane & 7, bcol = ((lane >> 3) & 1) * 8;
+    const bool bvalid = rb < NR && gc0 + rb % C < a.G;
+    // rows past R and W_c rows past the cluster's valid groups read row 0: their
+    // products land in accumulator entries that are never used
+    const uint32_t abase = smem_u32(xs + size_t(arow < a.R ? arow : 0) * pitch + 2 * acol);
+    const uint32_t bbase = smem_u32(wsm + size_t(bvalid ? rb : 0) * pitch + 2 * bcol);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (s0 < s1) {
+      if (!mbar_wait(&bar[st], 0)) record_error(a.err, kDevErrConv);
+      for (int k = s0; k < s1; ++k) {
+        uint32_t af[4], bfr[2];
+        ldsm_x4(abase + 32u * k, af);
+        ldsm_x2(bbase + 32u * k, bfr);
+        mma_16816_bf16(acc, af, bfr);
+      }
+    }
+    // acc: (position g, rows 2t, 2t+1), (position g+8, rows 2t, 2t+1)
+    const int g = lane >> 2, t = lane & 3;
+    float* rw = red + warp * 128;
+    *reinterpret_cast<float2*>(rw + g * 8 + 2 * t) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(rw + (g + 8) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
+  }
+  if constexpr (C > 1) cluster_wait_acquire();  // the peers' barriers are initialised
+  __syncthreads();
+  // ---- warp partials summed (warp order), row r sent to the CTA mixing group gc0 + r % C ----
+  if (tid < 16 * NR) {
+    const int p = tid / NR, r = tid % NR;
+    if (p < a.R) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) v += red[w * 128 + p * 8 + r];
+      float* slot = recv + (rank * 2 + r / C) * 16 + p;
+      if constexpr (C > 1) {
+        if (gc0 + r % C < a.G) st_async_f32(slot, static_cast<uint32_t>(r % C), v, &bar[2]);
+      } else {
+        *slot = v;
+      }
+    }
+  }
+  if constexpr (C == 1) __syncthreads();
+  if (!mixer) return;
+  if constexpr (C > 1) {
+    if (!mbar_wait_cluster(&bar[2], 0)) record_error(a.err, kDevErrConv);
+  }
+  // ---- the 2-tap mix of 8 channels at position p ----
+  const int pm = tid >> 1;
+  float c0 = 0.f, c1 = 0.f;
+#pragma unroll
+  for (int k = 0; k < C; ++k) {  // rank order: deterministic
+    c0 += recv[(k * 2 + 0) * 16 + pm];
+    c1 += recv[(k * 2 + 1) * 16 + pm];
+  }
+  float ft[8], fm[8];
+  bf8_to_f32(xt, ft);
+  bf8_to_f32(xm, fm);
+  const float k0v[8] = {b0[0].x, b0[0].y, b0[0].z, b0[0].w, b0[1].x, b0[1].y, b0[1].z, b0[1].w};
+  const float k1v[8] = {b1[0].x, b1[0].y, b1[0].z, b1[0].w, b1[1].x, b1[1].y, b1[1].z, b1[1].w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float lo = fmaf(k0v[2 * q] + c0, ft[2 * q], (k1v[2 * q] + c1) * fm[2 * q]);
+    const float hi =
+        fmaf(k0v[2 * q + 1] + c0, ft[2 * q + 1], (k1v[2 * q + 1] + c1) * fm[2 * q + 1]);
+    const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+    ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
+  }
+  *reinterpret_cast<uint4*>(a.y + size_t(pm) * d + 16 * gmix + 8 * (tid & 1)) =
+      make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
+bool g_conv_gemv_attr[64][3];
+
+// Cluster size of the GEMV kernel: the largest of 4, 2, 1 whose slices fit the
+// shared-memory budget and whose K slice is still at least 256 long (each CTA
+// reads its slice of every position of x, so a cluster cuts the bytes each SM
+// waits for); 0 if none fits.
+int gemv_cluster(int d, int G) {
+  auto fits = [&](int C) {
+    return d % (16 * C) == 0 && G >= C && gemv_smem_bytes(d, C) <= kGvSmemMax;
+  };
+#ifdef DFL2_GEMV_C
+  if (fits(DFL2_GEMV_C)) return DFL2_GEMV_C;
+#endif
+  for (int C = 4; C >= 1; C >>= 1)
+    if (fits(C) && (C == 1 || d / C >= 256)) return C;
+  return 0;
+}
+
+template <int C>
+cudaError_t launch_gemv_c(const ConvGemvArgs& a, cudaStream_t s, int dev) {
+  auto k = conv_gemv_kernel<C>;
+  constexpr int ci = C == 1 ? 0 : (C == 2 ? 1 : 2);
+  if (!g_conv_gemv_attr[dev & 63][ci]) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kGvSmemMax));
+    if (e != cudaSuccess) return e;
+    g_conv_gemv_attr[dev & 63][ci] = true;
+  }
+  const int grid = (a.G + C - 1) / C * C;
+  return launch_kc(k, dim3(grid), dim3(kGvThreads), gemv_smem_bytes(a.d, C), s, true, C, a);
+}
+
 
 }  // namespace
 
@@ -501,6 +770,13 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   }
   const int sms = device_info().sms;
   const int R = B * L;
+  const int gv_c = R <= kGvMaxR ? gemv_cluster(d, d / kGroup) : 0;
+  if (gv_c > 0) {
+    // ---- at most 16 positions: the GEMV kernel, one group per CTA ----
+    const ConvGemvArgs g{x, x_prev, base, W_c, y, R, L, d, d / kGroup, device_error_word()};
+    return gv_c == 4 ? launch_gemv_c<4>(g, s, dev)
+                     : (gv_c == 2 ? launch_gemv_c<2>(g, s, dev) : launch_gemv_c<1>(g, s, dev));
+  }
   if (R <= kSMaxRows && d % kCBK == 0 && d / kGroup >= kSGroups / 2) {
     // ---- few positions: the transposed kernel ----
     if (!g_conv_small_attr[dev & 63]) {
