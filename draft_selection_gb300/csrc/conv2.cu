@@ -44,6 +44,7 @@ struct ConvArgs {
   __nv_bfloat16* y;             // [R, d]
   int R, L, d, G;
   int NG, ntiles, splits, kps, kblocks, stages;
+  int side;  // K blocks whose x tile is kept for the mix (the CTA's own channels), or 0
   uint32_t* err;
 };
 
@@ -62,10 +63,22 @@ __host__ __device__ constexpr size_t conv_stage_area(int NG, int stages) {
 __host__ __device__ constexpr size_t conv_recv_bytes(int NG, int splits) {
   return splits > 1 ? size_t(kCBM + kCMaxSplits) * conv_pitch(NG) * 4 : 0;
 }
-__host__ __device__ constexpr size_t conv_smem_bytes(int NG, int stages, int splits) {
-  // [operand stages | corrections] [receive slots] [base slice] [barriers]
-  return 1024 + conv_stage_area(NG, stages) + conv_recv_bytes(NG, splits) +
-         size_t(2) * 16 * NG * 4 + 256;
+__host__ __device__ constexpr size_t conv_smem_bytes(int NG, int stages, int splits, int side) {
+  // [operand stages | corrections] [kept x tiles] [receive slots] [base slice] [barriers]
+  return 1024 + conv_stage_area(NG, stages) + size_t(side) * kCAStage +
+         conv_recv_bytes(NG, splits) + size_t(2) * 16 * NG * 4 + 256;
+}
+
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bf8_unpack(const uint4 v, float f[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    f[2 * q] = __uint_as_float(w[q] << 16);
+    f[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+  }
 }
 
 // Warp roles: 0 = TMA producer (one thread), 1 = TMEM owner and MMA issuer (one
@@ -82,7 +95,9 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   uint8_t* sA = smem;                                   // [stages][128 rows][128 B]
   uint8_t* sB = smem + size_t(nst) * kCAStage;          // [stages][2*NG rows][128 B]
   float* corr = reinterpret_cast<float*>(smem);         // [128][pitch], after the mainloop
-  float* recv = reinterpret_cast<float*>(smem + conv_stage_area(NG, nst));  // [S][rows_per][pitch]
+  // x tiles of the K blocks that hold this CTA's own channels, kept for the mix
+  uint8_t* sKeep = smem + conv_stage_area(NG, nst);                      // [side][128 rows][128 B]
+  float* recv = reinterpret_cast<float*>(sKeep + size_t(a.side) * kCAStage);  // [S][rows_per][pitch]
   float* bslice = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(recv) +
                                            conv_recv_bytes(NG, a.splits));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * NG);
@@ -98,6 +113,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   const int kb0 = split * a.kps;
   const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;  // >= 1 by construction on the host
   const uint32_t ncols = N < 32 ? 32u : static_cast<uint32_t>(N);
+  const int kbk0 = (16 * g0) / kCBK;  // first K block of this CTA's channels
 
   if (tid == 0) {
     for (int s = 0; s < nst; ++s) {
@@ -121,9 +137,13 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       const uint32_t tx = static_cast<uint32_t>(kCAStage + bst);
       for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
         if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrConv);
-        const int k0 = (kb0 + it) * kCBK;
+        const int kb = kb0 + it;
+        const int k0 = kb * kCBK;
+        const int keep = kb - kbk0;  // in [0, side): this x tile stays for the mix
         mbar_arrive_expect_tx(&full_bar[s], tx);
-        tma_load_2d(sA + size_t(s) * kCAStage, &tmX, k0, m0, &full_bar[s]);
+        tma_load_2d(keep >= 0 && keep < a.side ? sKeep + size_t(keep) * kCAStage
+                                               : sA + size_t(s) * kCAStage,
+                    &tmX, k0, m0, &full_bar[s]);
         uint8_t* dB = sB + size_t(s) * bst;
         tma_load_2d(dB, &tmW, k0, g0, &full_bar[s]);
         tma_load_2d(dB + NG * 128, &tmW, k0, a.G + g0, &full_bar[s]);
@@ -140,7 +160,9 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
       for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
         if (!mbar_wait(&full_bar[s], ph)) record_error(a.err, kDevErrConv);
         tc_fence_after();
-        const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kCAStage);
+        const int keep = kb0 + it - kbk0;
+        const uint64_t ad = umma_desc_sw128(keep >= 0 && keep < a.side ? sKeep + size_t(keep) * kCAStage
+                                                                       : sA + size_t(s) * kCAStage);
         const uint64_t bd = umma_desc_sw128(sB + size_t(s) * bst);
 #pragma unroll
         for (int k = 0; k < kCBK / 16; ++k)
@@ -221,6 +243,81 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
   }
   pdl_launch_dependents();
 
+  if (a.side) {
+    // ---- the 2-tap mix from the kept tiles: thread = (group, half of its 16
+    // channels), base in registers, down a run of consecutive rows (x_{t-1} is
+    // the previous row's x_t), four rows at a time so that their arithmetic
+    // overlaps.  The host takes this path only when L >= run, so a run holds at
+    // most one position t = 0 (x_{t-1} = x_prev); that row and the row above the
+    // run are the only loads from global memory, issued before the loop. ----
+    const int q = tid % (2 * NG), gl = q >> 1, h = q & 1;
+    const int groups = kCThreads / (2 * NG);
+    const int run = (kCBM + groups - 1) / groups;
+    const int g = g0 + gl;
+    const int lr0 = (tid / (2 * NG)) * run;
+    const int lend = min(min(lr0 + run, kCBM), a.R - m0);
+    if (tid < groups * 2 * NG && g < a.G && lr0 < lend) {
+      const int c = 16 * g + 8 * h;  // first of this thread's 8 channels
+      const int ch = c - kCBK * kbk0;  // channel within the kept tiles
+      const uint8_t* tile = sKeep + size_t(ch / kCBK) * kCAStage;
+      const int j = (ch % kCBK) / 8;
+      auto kept = [&](int row) {
+        return *reinterpret_cast<const uint4*>(tile + row * 128 + ((j ^ (row & 7)) << 4));
+      };
+      const int t0 = (m0 + lr0) % a.L;
+      const int tz = t0 == 0 ? 0 : a.L - t0;  // offset of the run's t = 0 row, if < run
+      uint4 xp = make_uint4(0u, 0u, 0u, 0u);
+      if (lr0 + tz < lend)
+        xp = __ldcg(reinterpret_cast<const uint4*>(a.x_prev + size_t((m0 + lr0 + tz) / a.L) * a.d + c));
+      uint4 prev = xp;  // x_{t-1} of the first row
+      if (t0 != 0)
+        prev = lr0 > 0 ? kept(lr0 - 1)
+                       : __ldcg(reinterpret_cast<const uint4*>(a.x + size_t(m0 - 1) * a.d + c));
+      float b0[8], b1[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        b0[i] = bslice[(8 * h + i) * NG + gl];
+        b1[i] = bslice[16 * NG + (8 * h + i) * NG + gl];
+      }
+      constexpr int kU = 4;
+      for (int lr = lr0; lr < lend; lr += kU) {
+        uint4 xt[kU], xm[kU];
+        float c0[kU], c1[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int row = min(lr + u, lend - 1);
+          xt[u] = kept(row);
+          c0[u] = corr[size_t(row) * pitch + gl];
+          c1[u] = corr[size_t(row) * pitch + NG + gl];
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          xm[u] = (lr + u - lr0 == tz) ? xp : (u == 0 ? prev : xt[u - 1]);
+        }
+        prev = xt[kU - 1];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          if (lr + u >= lend) break;
+          float ft[8], fm[8];
+          bf8_unpack(xt[u], ft);
+          bf8_unpack(xm[u], fm);
+          uint32_t ow[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float lo =
+                fmaf(b0[2 * i] + c0[u], ft[2 * i], (b1[2 * i] + c1[u]) * fm[2 * i]);
+            const float hi = fmaf(b0[2 * i + 1] + c0[u], ft[2 * i + 1],
+                                  (b1[2 * i + 1] + c1[u]) * fm[2 * i + 1]);
+            const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+            ow[i] = *reinterpret_cast<const uint32_t*>(&pr);
+          }
+          *reinterpret_cast<uint4*>(a.y + size_t(m0 + lr + u) * a.d + c) =
+              make_uint4(ow[0], ow[1], ow[2], ow[3]);
+        }
+      }
+    }
+    return;
+  }
   // ---- the 2-tap mix: one (row, group) = 16 channels per item, 4 items per pass ----
   constexpr int kBatch = 4;
   const int items = r_n * NG;
@@ -527,9 +624,6 @@ __host__ __device__ constexpr size_t gemv_smem_bytes(int d, int C) {
   return size_t(16 + 2 * C) * gemv_pitch(d, C) + 8 * 16 * 8 * 4 + size_t(C) * 2 * 16 * 4 + 32;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -837,10 +931,16 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   a.kps = (a.kblocks + want - 1) / want;
   a.splits = (a.kblocks + a.kps - 1) / a.kps;  // every split gets at least one K block
   if (a.splits > 1 && NG != 16) return cudaErrorInvalidConfiguration;  // receive slots need NG 16
+  // One CTA per SM without split K: the x tiles of the CTA's own channels stay
+  // in shared memory for the mix (at most 4 K blocks, 64 KB).
+  a.side = 0;
+  if (a.splits == 1 && (long long)tiles <= sms && (16 * NG) % kCBK == 0 && 16 * NG / kCBK <= 4 &&
+      a.d % kCBK == 0 && L >= NG)  // L >= the mix's run of rows (NG)
+    a.side = 16 * NG / kCBK;
   // As many operand stages as the shared memory of one CTA per SM holds, or of
   // two when the tiles outnumber the SMs; never more than the K blocks.
   const size_t budget = (long long)tiles * a.splits > sms ? size_t(112) * 1024 : kCSmemMax;
-  const size_t fixed = conv_smem_bytes(NG, 0, a.splits) - conv_stage_area(NG, 0);
+  const size_t fixed = conv_smem_bytes(NG, 0, a.splits, a.side) - conv_stage_area(NG, 0);
   const size_t per_stage = size_t(kCAStage) + conv_bstage_bytes(NG);
   int stages = budget > fixed ? static_cast<int>((budget - fixed) / per_stage) : 2;
   stages = std::max(2, std::min({stages, kCMaxStages, std::max(a.kps, 2)}));
@@ -850,7 +950,8 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
       !tensor_map_bf16(W_c, uint64_t(2) * a.G, uint64_t(d), static_cast<uint32_t>(NG), &tmW))
     return cudaErrorInvalidValue;
   return launch_kc(conv_tc_kernel, dim3(tiles * a.splits), dim3(kCThreads),
-                   conv_smem_bytes(NG, stages, a.splits), s, true, a.splits, a, tmX, tmW);
+                   conv_smem_bytes(NG, stages, a.splits, a.side), s, true, a.splits, a, tmX,
+                   tmW);
 }
 
 }  // namespace dfl2

@@ -64,7 +64,8 @@ def test_batched_workloads(name, nseq):
 
 @pytest.mark.parametrize("B,L,d", [(1, 1, 16), (1, 17, 48), (3, 5, 1024), (2, 33, 6144),
                                    (4, 16, 2560), (1, 2, 10240), (2, 8, 2560), (1, 16, 48),
-                                   (1, 3, 32), (1, 4, 20480), (16, 1, 2560)])
+                                   (1, 3, 32), (1, 4, 20480), (16, 1, 2560), (5, 16, 2560),
+                                   (3, 50, 512), (9, 17, 4096), (70, 16, 2560)])
 def test_edge_shapes(B, L, d):
     w = wl.WORKLOADS["tiny_l8_v32k"].with_(B=B, L=L, d=d)
     c = wl.make_conv_inputs(w, 3, "cpu")
