@@ -106,6 +106,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if (clock64() - t0 > kWaitCycles) return false;
   }
 }
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+// 4-byte store into distributed shared memory (an address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void cluster_arrive_release() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
@@ -515,6 +525,40 @@ __device__ __forceinline__ float walk_uniform(uint64_t seed, uint64_t cycle, int
 // T > 0: p_j = exp((S_j - max)/T), Z = sum in slot order, the first j with
 // u Z < p_0 + ... + p_j (else the last j with p_j > 0), q = p / Z.  `row` may
 // alias `q` (the row is read completely first).
+// The same decision taken by the 16 lanes of a half-warp together, lane j
+// holding entry j of the row: the same operations in the same order as
+// walk_row_choice (the running sum is carried lane to lane in slot order, so Z
+// and every partial sum are bit for bit the sequential ones), with short
+// dependency chains and little code.  Every lane of the warp must call it
+// (both halves, same T).  Returns the pick; q_j is lane j's probability.
+__device__ __forceinline__ int walk_row_choice16(float v, float T, float u, float& q_j) {
+  const int lane = threadIdx.x & 31, j = lane & 15, hbase = lane & 16;
+  float m = v;
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off, 16));
+  if (T == 0.f) {
+    const uint32_t eq = (__ballot_sync(0xffffffffu, v == m) >> hbase) & 0xFFFFu;
+    const int pick = __ffs(eq) - 1;  // the first maximum, as the sequential scan keeps
+    q_j = j == pick ? 1.f : 0.f;
+    return pick;
+  }
+  const float p = expf((v - m) / T);
+  float cum = p;
+#pragma unroll 1
+  for (int s = 1; s < kCand; ++s) {  // cum_s = cum_{s-1} + p_s, in slot order
+    const float prev = __shfl_up_sync(0xffffffffu, cum, 1, 16);
+    if (j == s) cum = prev + p;
+  }
+  const float Z = __shfl_sync(0xffffffffu, cum, 15, 16);
+  const float uZ = u * Z;
+  // both votes by every lane (the halves may take different branches below)
+  const uint32_t hit = (__ballot_sync(0xffffffffu, uZ < cum) >> hbase) & 0xFFFFu;
+  const uint32_t pos = (__ballot_sync(0xffffffffu, p > 0.f) >> hbase) & 0xFFFFu;
+  // the first crossing; if rounding left none, the last slot with mass
+  const int pick = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : 0);
+  q_j = p / Z;
+  return pick;
+}
 __device__ __forceinline__ int walk_row_choice(const float* row, float T, float u, float* q) {
   float v[kCand];
 #pragma unroll

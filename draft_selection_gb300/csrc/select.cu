@@ -451,6 +451,264 @@ __global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
   pdl_launch_dependents();
 }
 
+// ============================================================================
+// Pair scores with the walk fused, one thread-block cluster per sequence.
+// ============================================================================
+// CTA `rank` of the cluster of sequence b takes positions rank*P .. rank*P+P-1,
+// one 128-thread group per position (the same computation as pair16_kernel).
+// Each group takes the walk's decision for every predecessor row of its
+// position and stores the choices, the q rows and its 16 candidate tokens
+// straight into the shared memory of the cluster's first CTA (distributed
+// shared memory, about 1 KB per position); after one cluster barrier that CTA
+// follows the chosen slots from the verified token and writes the path.  No
+// global workspace, fence or ticket sits between the positions and the walk.
+constexpr int kPwMaxL = 32;  // P <= 4 positions per CTA, clusters of <= 8
+
+struct PairGroupSmem {
+  float Gs[kCand][kPairPitch];   // A(a_i) ⊙ H(h_t)
+  float Bsh[kCand][kPairPitch];  // B(b_j)
+  float Hs[kRank];
+  float U[kCand];
+  float Srow[kCand][kCand + 1];
+  float Shalf[kCand][kCand + 1];
+  const float* rowA[kCand];
+  const float* rowB[kCand];
+};
+struct PairWalkSmem {  // used in the cluster's first CTA only (same layout in every CTA)
+  float q[kPwMaxL][kCand][kCand];
+  int choice[kPwMaxL][kCand];
+  int tok[kPwMaxL][kCand];
+  int path[kPwMaxL];
+  uint64_t bar;  // counts the bytes stored by every position
+};
+
+// Stores into CTA `rank`'s shared memory at the offsets of `local` / `bar`,
+// counted as transaction bytes on that CTA's mbarrier.
+__device__ __forceinline__ void st_async_b32(const void* local, uint32_t rank, uint32_t v,
+                                             const uint64_t* bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(
+                   dsmem_addr(local, rank)),
+               "r"(v), "r"(dsmem_addr(bar, rank))
+               : "memory");
+}
+__device__ __forceinline__ void st_async_f32(const void* local, uint32_t rank, float v,
+                                             const uint64_t* bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+                   dsmem_addr(local, rank)),
+               "f"(v), "r"(dsmem_addr(bar, rank))
+               : "memory");
+}
+__device__ __forceinline__ void st_async_v4(const void* local, uint32_t rank, float4 v,
+                                            const uint64_t* bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          dsmem_addr(local, rank)),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(dsmem_addr(bar, rank))
+      : "memory");
+}
+
+// Scores of position t of sequence b into g->Srow (rows past the predecessors
+// are -inf) and, when requested, into a.scores.  `sync` is the group's barrier.
+template <typename Sync>
+__device__ __forceinline__ void pair_position(const PairArgs& a, int b, int t, int tid,
+                                              PairGroupSmem* g, Sync sync) {
+  const int cell = b * a.L + t;
+  const int npred = t == 0 ? 1 : kCand;
+  const size_t rowA0 =
+      size_t(b) * (kCand * (a.L - 1) + 1) + (t == 0 ? 0 : 1 + size_t(kCand) * (t - 1));
+  const size_t rowB0 = size_t(b) * kCand * a.L + size_t(kCand) * t;
+  if (tid < 2 * kCand) {
+    const int i = tid % kCand;
+    const bool isA = tid < kCand;
+    const float* src;
+    if (a.tabA) {
+      int tok = 0;
+      if (isA) {
+        if (i < npred)
+          tok = t == 0 ? a.verified[b] : a.cand_idx[(size_t(b) * a.L + (t - 1)) * kCand + i];
+      } else {
+        tok = a.cand_idx[(size_t(b) * a.L + t) * kCand + i];
+      }
+      if (tok < 0 || tok >= a.V) {  // never read outside the tables
+        record_error(a.err, kDevErrBadIndex);
+        tok = 0;
+      }
+      src = (isA ? a.tabA : a.tabB) + size_t(tok) * kRank;
+    } else {
+      src = isA ? a.PA + (rowA0 + i) * kRank : a.PB + (rowB0 + i) * kRank;
+    }
+    (isA ? g->rowA : g->rowB)[i] = src;
+  }
+  sync();
+  float4 va[8], vb[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = tid + kPairThreads * k;
+    const int i = e >> 6, q4 = e & 63;
+    va[k] = i < npred ? __ldcg(reinterpret_cast<const float4*>(g->rowA[i]) + q4)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    vb[k] = __ldcg(reinterpret_cast<const float4*>(g->rowB[i]) + q4);
+  }
+  float gh[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) gh[k] = __ldcg(a.GH + size_t(cell) * kRank + tid + kPairThreads * k);
+  if (tid < kCand) g->U[tid] = __ldcg(a.cand_val + size_t(cell) * kCand + tid);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) g->Hs[tid + kPairThreads * k] = 1.0f / (1.0f + expf(-gh[k]));
+  sync();  // Hs complete
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int e = tid + kPairThreads * k;
+    const int i = e >> 6, c = 4 * (e & 63);
+    const float4 h = *reinterpret_cast<const float4*>(&g->Hs[c]);
+    *reinterpret_cast<float4*>(&g->Gs[i][c]) =
+        make_float4(va[k].x * h.x, va[k].y * h.y, va[k].z * h.z, va[k].w * h.w);
+    *reinterpret_cast<float4*>(&g->Bsh[i][c]) = vb[k];
+  }
+  sync();
+  {
+    const int half = tid >> 6, tt = tid & 63;
+    const int ip = tt >> 3, jp = tt & 7;
+    const int q0 = half * (kRank / 2);
+    float4 s00 = make_float4(0.f, 0.f, 0.f, 0.f), s01 = s00, s10 = s00, s11 = s00;
+#pragma unroll 4
+    for (int q = q0; q < q0 + kRank / 2; q += 4) {
+      const float4 g0 = *reinterpret_cast<const float4*>(&g->Gs[ip][q]);
+      const float4 g1 = *reinterpret_cast<const float4*>(&g->Gs[ip + 8][q]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&g->Bsh[jp][q]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&g->Bsh[jp + 8][q]);
+      s00.x = fmaf(g0.x, b0.x, s00.x); s00.y = fmaf(g0.y, b0.y, s00.y);
+      s00.z = fmaf(g0.z, b0.z, s00.z); s00.w = fmaf(g0.w, b0.w, s00.w);
+      s01.x = fmaf(g0.x, b1.x, s01.x); s01.y = fmaf(g0.y, b1.y, s01.y);
+      s01.z = fmaf(g0.z, b1.z, s01.z); s01.w = fmaf(g0.w, b1.w, s01.w);
+      s10.x = fmaf(g1.x, b0.x, s10.x); s10.y = fmaf(g1.y, b0.y, s10.y);
+      s10.z = fmaf(g1.z, b0.z, s10.z); s10.w = fmaf(g1.w, b0.w, s10.w);
+      s11.x = fmaf(g1.x, b1.x, s11.x); s11.y = fmaf(g1.y, b1.y, s11.y);
+      s11.z = fmaf(g1.z, b1.z, s11.z); s11.w = fmaf(g1.w, b1.w, s11.w);
+    }
+    float (*dst)[kCand + 1] = half ? g->Shalf : g->Srow;
+    dst[ip][jp] = (s00.x + s00.y) + (s00.z + s00.w);
+    dst[ip][jp + 8] = (s01.x + s01.y) + (s01.z + s01.w);
+    dst[ip + 8][jp] = (s10.x + s10.y) + (s10.z + s10.w);
+    dst[ip + 8][jp + 8] = (s11.x + s11.y) + (s11.z + s11.w);
+  }
+  sync();
+  for (int e = tid; e < kCand * kCand; e += kPairThreads) {
+    const int i = e / kCand, j = e % kCand;
+    const float v = i < npred ? (g->Srow[i][j] + g->Shalf[i][j]) + g->U[j] : -INFINITY;
+    g->Srow[i][j] = v;
+    if (a.scores) a.scores[size_t(cell) * kCand * kCand + e] = v;
+  }
+  sync();
+}
+
+template <int P>
+__global__ void __launch_bounds__(kPairThreads * P) pair_walk_kernel(PairArgs a) {
+  extern __shared__ __align__(16) uint8_t pw_smem[];
+  const int grp = threadIdx.x / kPairThreads, tid = threadIdx.x % kPairThreads;
+  const int CL = (a.L + P - 1) / P;  // the cluster size
+  const int b = blockIdx.x / CL;
+  const int rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int t = rank * P + grp;
+  const bool live = t < a.L;
+  PairGroupSmem* g = reinterpret_cast<PairGroupSmem*>(pw_smem) + grp;
+  PairWalkSmem* w = reinterpret_cast<PairWalkSmem*>(pw_smem + P * sizeof(PairGroupSmem));
+  if (threadIdx.x == 0 && CL > 1) {
+    mbar_init(&w->bar, 1);
+    fence_mbar_init();
+    // every position's choices, q rows and tokens, in bytes (stored with st.async)
+    if (rank == 0)
+      mbar_arrive_expect_tx(&w->bar, uint32_t(kCand * 4 + 1 * (4 + kCand * 4)) +
+                                         uint32_t(a.L - 1) * uint32_t(kCand * 4 + kCand * (4 + kCand * 4)));
+  }
+  if (CL > 1)
+    cluster_arrive_release();  // the first CTA's barrier is initialised before any store
+  else
+    __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
+  // the walk's random number for this position, in flight during the scores
+  const float u = live && a.T > 0.f ? walk_uniform(__ldcg(a.seeds + b), a.cycle, t) : 0.f;
+  auto sync = [grp]() { named_sync(1 + grp, kPairThreads); };
+  if (live) pair_position(a, b, t, tid, g, sync);
+  // ---- the walk's decision for every predecessor row of position t, and the
+  // candidate tokens, into the first CTA (st.async, counted on its barrier) ----
+  if (CL > 1) cluster_wait_acquire();
+  if (live) {
+    const int npred = t == 0 ? 1 : kCand;
+    const int cell = b * a.L + t;
+    const int j = tid & 15;
+    // 16 lanes per predecessor row, 8 rows per pass
+#pragma unroll 1
+    for (int i = tid >> 4; i < kCand; i += kPairThreads / 16) {
+      float q_j;
+      const int c = walk_row_choice16(g->Srow[i][j], a.T, u, q_j);
+      if (i < npred) {
+        if (CL > 1) {
+          st_async_f32(&w->q[t][i][j], 0u, q_j, &w->bar);
+          if (j == 0) st_async_b32(&w->choice[t][i], 0u, static_cast<uint32_t>(c), &w->bar);
+        } else {  // a single CTA (no cluster launch): plain stores
+          w->q[t][i][j] = q_j;
+          if (j == 0) w->choice[t][i] = c;
+        }
+      }
+    }
+    if (tid < kCand) {
+      const int tok = __ldcg(a.cand_idx + size_t(cell) * kCand + tid);
+      if (CL > 1)
+        st_async_b32(&w->tok[t][tid], 0u, static_cast<uint32_t>(tok), &w->bar);
+      else
+        w->tok[t][tid] = tok;
+    }
+  }
+  if (CL == 1) __syncthreads();
+  if (rank != 0) return;
+  // ---- first CTA: follow the chosen slots from the verified token ----
+  if (threadIdx.x == 0) {
+    if (CL > 1 && !mbar_wait_cluster(&w->bar, 0)) record_error(a.err, kDevErrGemm);
+    int prev = 0;
+    for (int tt = 0; tt < a.L; ++tt) {
+      prev = w->choice[tt][prev] & (kCand - 1);
+      w->path[tt] = prev;
+    }
+  }
+  __syncthreads();
+  for (int tt = threadIdx.x; tt < a.L; tt += blockDim.x) {
+    const size_t c2 = size_t(b) * a.L + tt;
+    a.tokens[c2] = w->tok[tt][w->path[tt]];
+    if (a.slots) a.slots[c2] = w->path[tt];
+  }
+  if (a.q) {
+    for (int e = threadIdx.x; e < a.L * kCand; e += blockDim.x) {
+      const int tt = e / kCand, k = e % kCand;
+      const int row = tt == 0 ? 0 : w->path[tt - 1];  // step tt draws from its predecessor's row
+      a.q[(size_t(b) * a.L + tt) * kCand + k] = w->q[tt][row][k];
+    }
+  }
+}
+
+bool g_pw_attr[64][3];
+
+// The fused pair + walk launch: clusters of ceil(L / P) CTAs per sequence, P
+// the smallest of 1, 2, 4 that keeps the cluster within 8; L <= 32.
+cudaError_t launch_pair_walk(const PairArgs& qa, int B, int L, cudaStream_t s, bool pdl) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const int P = L <= 8 ? 1 : (L <= 16 ? 2 : 4);
+  const int CL = (L + P - 1) / P;
+  const size_t smem = size_t(P) * sizeof(PairGroupSmem) + sizeof(PairWalkSmem);
+  const int pi = P == 1 ? 0 : (P == 2 ? 1 : 2);
+  auto kern = P == 1 ? pair_walk_kernel<1> : (P == 2 ? pair_walk_kernel<2> : pair_walk_kernel<4>);
+  if (!g_pw_attr[dev & 63][pi]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    g_pw_attr[dev & 63][pi] = true;
+  }
+  return launch_kc(kern, dim3(B * CL), dim3(kPairThreads * P), smem, s, pdl, CL, qa);
+}
+
 bool g_gemm_attr[64];
 
 }  // namespace
@@ -636,6 +894,7 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
     qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
     qa.qrows = reinterpret_cast<float*>(w + p.q_off);
+    if (p.L <= kPwMaxL) return launch_pair_walk(qa, p.B, p.L, s, pdl);
   }
   return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
 }
@@ -688,6 +947,7 @@ cudaError_t launch_pair_tables(const SelectPlan& p, const int32_t* cand_idx, con
     qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
     qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
     qa.qrows = reinterpret_cast<float*>(w + p.q_off);
+    if (p.L <= kPwMaxL) return launch_pair_walk(qa, p.B, p.L, s, pdl);
   }
   return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
 }
