@@ -46,6 +46,7 @@ constexpr uint32_t kTmemCols = 256;
 enum RowKind : int { kRowsPA = 0, kRowsPB = 1, kRowsHidden = 2, kRowsE = 3 };
 
 struct GemmProblem {
+  const __nv_bfloat16* W;  // [256, d] (the L2 prefetch; the GEMM reads it through the tensor map)
   int kind;     // RowKind
   int M;        // rows
   int mtiles;   // ceil(M / 128)
@@ -121,6 +122,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tma_prefetch_desc(tmap);
   }
   if (warp == 4) tmem_alloc(tmem_slot, kTmemCols);
+  // This CTA's K range of the 256 W rows into L2 while the previous kernel
+  // (the top-16) still runs: a prefetch into L2 is coherent with writes in
+  // flight, so it may precede the dependency wait.
+  // One CTA per K range (the problem's first row tile) asks for it.
+  if (P.W && nkb > 0 && m0 == 0)
+    prefetch_l2_rows(P.W + size_t(tid) * a.d + size_t(kb0) * kBK, uint32_t(nkb) * kBK * 2u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -210,50 +217,77 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // ---- split K over the cluster: every CTA stores its fp32 partial tile to the
   // workspace (L2), then each CTA sums one slice of rows over the splits in rank
   // order (deterministic) and writes the result ----
+  // The partial tile goes TMEM -> shared memory (the drained operand stages,
+  // rows kStagePitch floats apart) -> global memory in whole rows, so that each
+  // warp store covers 512 contiguous bytes.
+  constexpr int kStagePitch = kBN + 4;
+  static_assert(size_t(kBM) * kStagePitch * 4 <= size_t(kGStages) * (kAStage + kBStage),
+                "the partial tile fits the operand stages");
   const int S = a.splits;
   float* mypart = P.part + (size_t(split) * P.M) * kBN;
+  float* stage = reinterpret_cast<float*>(smem);
   if (warp >= 4) {
     const int quarter = warp & 3;
-    const int row = m0 + quarter * 32 + lane;
+    const int lrow = quarter * 32 + lane;
 #pragma unroll 1
     for (int c = 0; c < kBN / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
-      if (row < P.M) {
-        float4* o = reinterpret_cast<float4*>(mypart + size_t(row) * kBN + c * 32);
+      float4* o = reinterpret_cast<float4*>(stage + size_t(lrow) * kStagePitch + c * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-      }
+      for (int q = 0; q < 8; ++q) o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
   }
   tc_fence_before();
+  __syncthreads();
+  {
+    const int rows = max(0, min(kBM, P.M - m0));
+    for (int e = tid; e < rows * (kBN / 4); e += kGemmThreads) {
+      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
+      *reinterpret_cast<float4*>(mypart + size_t(m0 + lr) * kBN + 4 * c4) =
+          *reinterpret_cast<const float4*>(stage + size_t(lr) * kStagePitch + 4 * c4);
+    }
+  }
   cluster_sync_all();  // every split's partial tile is in the workspace
   if (warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // the next launch may start now (it waits for this grid to finish before
+  // reading anything, and holds no tensor memory)
+  pdl_launch_dependents();
   const int per = (kBM + S - 1) / S;
   const int r0 = split * per;
   const int valid_rows = max(0, min(min(per, kBM - r0), P.M - (m0 + r0)));
   const int n4 = valid_rows * (kBN / 4);
   constexpr int kMaxSplitLoads = kMaxClusterSplits;
-  for (int e = tid; e < n4; e += kGemmThreads) {
-    const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
-    const size_t at = size_t(m0 + r0 + lr) * kBN + 4 * c4;
-    float4 v[kMaxSplitLoads];
+  constexpr int kPer = 2;  // elements per thread and pass: 2 x 8 loads in flight
+  for (int e0 = tid; e0 < n4; e0 += kGemmThreads * kPer) {
+    float4 v[kPer][kMaxSplitLoads];
 #pragma unroll
-    for (int k = 0; k < kMaxSplitLoads; ++k)  // every split's value requested first
-      v[k] = k < S ? __ldcg(reinterpret_cast<const float4*>(P.part + size_t(k) * P.M * kBN + at))
-                   : make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 acc = v[0];
+    for (int u = 0; u < kPer; ++u) {
+      const int e = e0 + u * kGemmThreads;
+      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
+      const size_t at = size_t(m0 + r0 + lr) * kBN + 4 * c4;
 #pragma unroll
-    for (int k = 1; k < kMaxSplitLoads; ++k) {  // rank order: deterministic
-      acc.x += v[k].x; acc.y += v[k].y; acc.z += v[k].z; acc.w += v[k].w;
+      for (int k = 0; k < kMaxSplitLoads; ++k)  // every split's value requested first
+        v[u][k] = k < S && e < n4
+                      ? __ldcg(reinterpret_cast<const float4*>(P.part + size_t(k) * P.M * kBN + at))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    *reinterpret_cast<float4*>(P.out + at) = acc;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int e = e0 + u * kGemmThreads;
+      if (e >= n4) break;
+      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
+      float4 acc = v[u][0];
+#pragma unroll
+      for (int k = 1; k < kMaxSplitLoads; ++k) {  // rank order: deterministic
+        acc.x += v[u][k].x; acc.y += v[u][k].y; acc.z += v[u][k].z; acc.w += v[u][k].w;
+      }
+      *reinterpret_cast<float4*>(P.out + size_t(m0 + r0 + lr) * kBN + 4 * c4) = acc;
+    }
   }
-  pdl_launch_dependents();
 }
 
 struct PairArgs {
@@ -796,6 +830,7 @@ static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, 
     const bool live = i < njobs;
     const __nv_bfloat16* W = live ? jobs[i].W : jobs[0].W;
     if (!tensor_map_bf16(W, kRank, d, kBN, &tm[i])) return cudaErrorInvalidValue;
+    g.prob[i].W = W;
     g.prob[i].kind = live ? jobs[i].kind : kRowsHidden;
     g.prob[i].M = live ? jobs[i].M : 0;
     g.prob[i].mtiles = live ? (jobs[i].M + kBM - 1) / kBM : 0;
@@ -849,7 +884,9 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   float* outs[3] = {PA, PB, GH};
   float* part = reinterpret_cast<float*>(w + p.part_off);
   int before = 0;
+  const __nv_bfloat16* Ws[3] = {W_A, W_B, W_H};
   for (int i = 0; i < 3; ++i) {
+    g.prob[i].W = Ws[i];
     g.prob[i].kind = i;
     g.prob[i].M = Ms[i];
     g.prob[i].mtiles = (Ms[i] + kBM - 1) / kBM;
