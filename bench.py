@@ -41,8 +41,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
     ("topk", "serving_b64"): 314433792,     # topk16_kernel_serving_b64.md
-    ("conv", "drafter4b_l16"): 1785088,     # conv_small_drafter4b_l16.md
-    ("conv", "serving_b64"): 7277056,       # conv_tc_serving_b64.md
+    ("conv", "drafter4b_l16"): 1759744,     # conv_gemv_drafter4b_l16.md
+    ("conv", "serving_b64"): 7287808,       # conv_tc_serving_b64.md
     ("lmhead", "drafter4b_l16"): 781673728,  # lmhead_topk_kernel_drafter4b_l16.md
     ("lmhead", "serving_b64"): 786832384,    # lmhead_topk_kernel_serving_b64.md
 }
@@ -286,13 +286,18 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
     case.select()
     g_walk, _ = capture(case.walk)
     g_conv, _ = capture(lambda: case.conv(0))
+    g_c20, _ = capture(case.convs20)
     sub = max(3, min(steps, 400))
     res = {"step": summarize(time_graph(g_step, steps, warmup, flush)),
            "tail": summarize(time_graph(g_tail, sub, warmup, flush)),
            "topk": summarize(time_graph(g_topk, sub, warmup, flush)),
            "select": summarize(time_graph(g_sel, sub, warmup, flush)),
            "walk": summarize(time_graph(g_walk, sub, warmup, flush)),
-           "conv": summarize(time_graph(g_conv, sub, warmup, flush))}
+           "conv_alone": summarize(time_graph(g_conv, sub, warmup, flush))}
+    # A conv call as it runs in the step: the graph of the block's conv calls
+    # back to back (one graph launch amortised over them), per call.
+    c20 = summarize(time_graph(g_c20, sub, warmup, flush))
+    res["conv"] = {k: v / w.conv_calls for k, v in c20.items()}
     res["kernels_per_step"] = k_step
     build_ms = case.build_tables()
     g_tt, _ = capture(case.tail_tables)
@@ -624,6 +629,7 @@ def main():
             "tail_blocks_per_s": round(world * wb.B / (tail_ms * 1e-3), 1),
             "step_us": round(step_b * 1e3, 2), "tail_us": round(tail_ms * 1e3, 2),
             "conv_us_per_call": round(rb["conv"]["mean_ms"] * 1e3, 2),
+            "conv_alone_us": round(rb["conv_alone"]["mean_ms"] * 1e3, 2),
             "tail_hbm_gbs": round(tb / (tail_ms * 1e-3) / 1e9, 1),
             "tail_frac_of_hbm": round(tb / (tail_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
             "tail_bytes": tb,
@@ -659,7 +665,7 @@ def main():
             "tail_us": round(res["tail"]["mean_ms"] * 1e3, 2),
             "conv20_us": round(res["conv"]["mean_ms"] * 1e3 * w.conv_calls, 2),
             "kernel_us": {k: round(res[k]["mean_ms"] * 1e3, 2) for k in
-                          ("topk", "select", "walk", "conv")},
+                          ("topk", "select", "walk", "conv", "conv_alone")},
             "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
             "per_kernel": res["per_kernel"],
             "tables": res["tables"],
