@@ -64,6 +64,9 @@ def load():
     L.dfl2_select.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, P, P, SZ, P]
     L.dfl2_walk.argtypes = [P, P, I, I, F, P, U64, P, P, P, P]
     L.dfl2_conv2.argtypes = [P, P, P, P, I, I, I, P, P]
+    L.dfl2_conv2_workspace_size.argtypes = [I, I, I]
+    L.dfl2_conv2_workspace_size.restype = SZ
+    L.dfl2_conv2_ws.argtypes = [P, P, P, P, I, I, I, P, P, SZ, P]
     L.dfl2_tail_workspace_size.argtypes = [I, I, I, I]
     L.dfl2_tail_workspace_size.restype = SZ
     L.dfl2_tail.argtypes = [P, I, P, P, P, P, P, P, I, I, I, I, F, P, U64, P, P, P, P, P, P,
@@ -78,7 +81,7 @@ def load():
     L.dfl2_verify_workspace_size.restype = SZ
     L.dfl2_verify.argtypes = [P, P, P, P, P, I, I, I, I, P, U64, P, P, P, SZ, P]
     for name in ("dfl2_workspace_init", "dfl2_device_error", "dfl2_topk", "dfl2_select",
-                 "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify", "dfl2_tables_build",
+                 "dfl2_walk", "dfl2_conv2", "dfl2_conv2_ws", "dfl2_tail", "dfl2_verify", "dfl2_tables_build",
                  "dfl2_select_tables", "dfl2_tail_tables"):
         getattr(L, name).restype = I
     _lib = L
@@ -247,6 +250,19 @@ def dfl2_conv2(x, x_prev, base, W_c, y, stream=None, *, dims=None) -> None:
     B, L, d = dims if dims is not None else x.shape
     _check(load().dfl2_conv2(_ptr(x), _ptr(x_prev), _ptr(base), _ptr(W_c), B, L, d, _ptr(y),
                              _stream(stream)))
+
+
+def dfl2_conv2_workspace_size(B: int, L: int, d: int) -> int:
+    return int(load().dfl2_conv2_workspace_size(B, L, d))
+
+
+def dfl2_conv2_ws(x, x_prev, base, W_c, y, ws, stream=None, *, dims=None, ws_bytes=None) -> None:
+    """dfl2_conv2 with a workspace of dfl2_conv2_workspace_size bytes (ws may be
+    None when that is 0): the split-K kernel for many positions."""
+    B, L, d = dims if dims is not None else x.shape
+    wb = ws_bytes if ws_bytes is not None else (_nbytes(ws) if ws is not None else 0)
+    _check(load().dfl2_conv2_ws(_ptr(x), _ptr(x_prev), _ptr(base), _ptr(W_c), B, L, d, _ptr(y),
+                                _ptr(ws), wb, _stream(stream)))
 
 
 def dfl2_tail(logits, verified_tok, hidden, E, W_A, W_B, W_H, temperature: float, seeds,

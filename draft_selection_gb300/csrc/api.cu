@@ -535,9 +535,10 @@ dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L
   return DFL2_OK;
 }
 
-dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
-                       const uint16_t* W_c, int B, int L, int d, uint16_t* y,
-                       dfl2_stream stream) {
+namespace {
+dfl2_status conv2_common(const uint16_t* x, const uint16_t* x_prev, const float* base,
+                         const uint16_t* W_c, int B, int L, int d, uint16_t* y, void* ws,
+                         size_t ws_bytes, bool with_ws, dfl2_stream stream) {
   DFL2_TRY(check_shape(B, L));
   if (d < dfl2::kGroup || d % dfl2::kGroup != 0 || d > 65536)
     return fail(DFL2_ERR_UNSUPPORTED, "d=%d: the conv needs a multiple of 16 up to 65536", d);
@@ -548,11 +549,43 @@ dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* b
     return fail(DFL2_ERR_INVALID_ARG, "y overlaps x or x_prev");
   DFL2_TRY(ensure_device());
   DFL2_TRY(check_device(ptrs));
+  void* use_ws = nullptr;
+  if (with_ws) {
+    const size_t need = dfl2::conv2_ws_bytes(B, L, d);
+    if (need > 0) {
+      DFL2_TRY(check_ws(ws, ws_bytes, need));
+      const Ptrs wp = {{ws, "ws"}};
+      DFL2_TRY(check_host(wp));
+      DFL2_TRY(check_device(wp));
+      if (overlaps(ws, need, y, ybytes) || overlaps(ws, need, x, ybytes))
+        return fail(DFL2_ERR_INVALID_ARG, "ws overlaps x or y");
+      use_ws = ws;
+    }
+  }
   cudaError_t e = dfl2::launch_conv2(bf(x), bf(x_prev), base, bf(W_c), B, L, d,
-                                     reinterpret_cast<__nv_bfloat16*>(y),
+                                     reinterpret_cast<__nv_bfloat16*>(y), use_ws,
                                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "conv launch");
   return DFL2_OK;
+}
+}  // namespace
+
+dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
+                       const uint16_t* W_c, int B, int L, int d, uint16_t* y,
+                       dfl2_stream stream) {
+  return conv2_common(x, x_prev, base, W_c, B, L, d, y, nullptr, 0, false, stream);
+}
+
+size_t dfl2_conv2_workspace_size(int B, int L, int d) {
+  if (B < 1 || L < 1 || d < dfl2::kGroup || d % dfl2::kGroup != 0 || d > 65536) return 0;
+  if (ensure_device() != DFL2_OK) return 0;
+  return dfl2::conv2_ws_bytes(B, L, d);
+}
+
+dfl2_status dfl2_conv2_ws(const uint16_t* x, const uint16_t* x_prev, const float* base,
+                          const uint16_t* W_c, int B, int L, int d, uint16_t* y, void* ws,
+                          size_t ws_bytes, dfl2_stream stream) {
+  return conv2_common(x, x_prev, base, W_c, B, L, d, y, ws, ws_bytes, true, stream);
 }
 
 size_t dfl2_tail_workspace_size(int B, int L, int V, int d) {

@@ -584,6 +584,353 @@ __global__ void __launch_bounds__(kCThreads, 1)
 bool g_conv_small_attr[64];
 
 // ============================================================================
+// Many positions: corr^T tiles of 128 W_c rows x up to 256 positions.
+// ============================================================================
+// The transposed product of the kernel above, now over tiles of Np <= 256
+// positions (the N of one tcgen05.mma at M = 128).  A tile pairs 64 groups
+// (their 128 W_c rows, both taps, as A) with Np positions (as B), so a position
+// tile's x rows are read once per 64 groups instead of once per narrow group
+// slice, and W_c once per position tile.  Both operands arrive by TMA (zero
+// fill past the last position and the last W_c row).  When the tiles do not
+// cover the GPU, K is split over a cluster of S CTAs and the partial tiles are
+// exchanged through a caller workspace in L2: each CTA stores its tile in
+// whole 128-byte row pieces, one cluster barrier (release / acquire), and CTA
+// s of the cluster sums, in rank order, the S slices of the rows of groups
+// [s*64/S, (s+1)*64/S) of the tile, the groups it mixes.  (The same exchange
+// over distributed shared memory was measured at about 6 us for the 128 KB
+// tiles of a 96-CTA launch, against 4 us for the whole mainloop; L2 delivers
+// several times the bandwidth.)  Each thread then mixes a run of 16
+// consecutive positions of 8 channels, loading the run's x rows at once and
+// carrying x_{t-1} in registers.
+constexpr int kPGroups = 64;     // groups per tile: 128 W_c rows (both taps) = M
+constexpr int kPMaxStages = 4;
+constexpr int kPRun = 16;        // consecutive positions mixed by one thread
+
+struct ConvPtileArgs {
+  const __nv_bfloat16* x;       // [R, d] (the mix; the GEMM reads x through tmX)
+  const __nv_bfloat16* x_prev;  // [B, d]
+  const float* base;            // [2, d]
+  __nv_bfloat16* y;             // [R, d]
+  float* ws;                    // [tiles][splits][128][Np] partials (splits > 1)
+  int R, L, d, G, Np, gtiles, splits, kps, kblocks, stages;
+  uint32_t* err;
+};
+
+__host__ __device__ constexpr size_t ptile_stage_bytes(int Np) {
+  return size_t(kCAStage) + size_t(Np) * 128;  // [128 W_c rows | Np x rows] x 128 B
+}
+__host__ __device__ constexpr int ptile_pitch(int Np) { return Np + 4; }  // fp32 per slot row
+constexpr size_t kPScratch = size_t(8) * 32 * 128;  // a 32 x 32 fp32 block per warp
+__host__ __device__ constexpr size_t ptile_max3(size_t a, size_t b, size_t c) {
+  return a > b ? (a > c ? a : c) : (b > c ? b : c);
+}
+// The operand ring; after the mainloop the same bytes hold the warps' transpose
+// blocks and, past them, the corrections of the CTA's groups (all 128 rows
+// when S = 1).
+__host__ __device__ constexpr size_t ptile_area(int Np, int stages) {
+  return ptile_max3(size_t(stages) * ptile_stage_bytes(Np),
+                    kPScratch + size_t(2 * kPGroups) * ptile_pitch(Np) * 4, 0);
+}
+// Partial tiles exchanged through the workspace: [tiles][S][128][Np] fp32.
+__host__ __device__ constexpr size_t ptile_ws_bytes(long long tiles, int S, int Np) {
+  return S > 1 ? size_t(tiles) * S * size_t(2 * kPGroups) * Np * 4 : 0;
+}
+__host__ __device__ constexpr size_t ptile_smem_bytes(int Np, int stages) {
+  // [ring | transpose blocks | corrections] [base slice, 2 x 16 x 64 f32] [barriers, TMEM slot]
+  return 1024 + ptile_area(Np, stages) + size_t(2) * 16 * kPGroups * 4 + 256;
+}
+
+// Warp roles in the mainloop: 0 = TMA producer (one thread), 1 = TMEM owner and
+// MMA issuer (one thread), 2-3 = the base slice.  Then all 8 warps drain TMEM
+// (warps w and w+4 share lane quarter w%4, alternate 32-column chunks) and mix.
+__global__ void __launch_bounds__(kCThreads, 2)
+    conv_ptile_kernel(const __grid_constant__ ConvPtileArgs a,
+                      const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmX) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const int S = a.splits, Np = a.Np, pitch = ptile_pitch(Np), nst = a.stages;
+  const int og = kPGroups / S;  // groups this CTA mixes
+  const int orows = 2 * og;     // their W_c rows (tap 0, then tap 1)
+  const size_t sbytes = ptile_stage_bytes(Np);
+  uint8_t* ring = smem;  // stage s: [W_c 16 KB][x Np x 128 B]
+  float* bslice = reinterpret_cast<float*>(smem + ptile_area(Np, nst));  // [2][16*og]
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(bslice + 2 * 16 * kPGroups);
+  uint64_t* empty_bar = full_bar + kPMaxStages;
+  uint64_t* accum_bar = empty_bar + kPMaxStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int split = blockIdx.x % S;
+  const int tile = blockIdx.x / S;
+  const int g0 = (tile % a.gtiles) * kPGroups;
+  const int p0 = (tile / a.gtiles) * Np;
+  const int kb0 = split * a.kps;
+  const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;  // >= 1 by construction on the host
+  const uint32_t ncols = Np <= 32 ? 32u : (Np <= 64 ? 64u : (Np <= 128 ? 128u : 256u));
+  const int gown = g0 + split * og;  // first group this CTA mixes
+
+  if (tid == 0) {
+    for (int st = 0; st < nst; ++st) {
+      mbar_init(&full_bar[st], 1);
+      mbar_init(&empty_bar[st], 1);
+    }
+    mbar_init(accum_bar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tmW);
+    tma_prefetch_desc(&tmX);
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, ncols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- producer: both taps' W_c rows and Np x rows by TMA ----
+      const uint32_t tx = static_cast<uint32_t>(sbytes);
+      for (int it = 0; it < nkb; ++it) {
+        const int st = it % nst;
+        if (it >= nst && !mbar_wait(&empty_bar[st], ((it / nst) - 1) & 1))
+          record_error(a.err, kDevErrConv);
+        const int k0 = (kb0 + it) * kCBK;
+        uint8_t* dst = ring + size_t(st) * sbytes;
+        mbar_arrive_expect_tx(&full_bar[st], tx);
+        tma_load_2d(dst, &tmW, k0, g0, &full_bar[st]);
+        tma_load_2d(dst + kCAStage / 2, &tmW, k0, a.G + g0, &full_bar[st]);
+        tma_load_2d(dst + kCAStage, &tmX, k0, p0, &full_bar[st]);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---- MMA issuer ----
+      const uint32_t idesc = umma_idesc_bf16(kCBM, Np);
+      for (int it = 0; it < nkb; ++it) {
+        const int st = it % nst;
+        if (!mbar_wait(&full_bar[st], (it / nst) & 1)) record_error(a.err, kDevErrConv);
+        tc_fence_after();
+        const uint64_t ad = umma_desc_sw128(ring + size_t(st) * sbytes);
+        const uint64_t bd = umma_desc_sw128(ring + size_t(st) * sbytes + kCAStage);
+#pragma unroll
+        for (int k = 0; k < kCBK / 16; ++k)
+          umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, (it > 0 || k > 0) ? 1u : 0u);
+        umma_commit(&empty_bar[st]);
+      }
+      umma_commit(accum_bar);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // idle during the mainloop: the base slice of the channels this CTA mixes
+    for (int e = tid - 64; e < 2 * 16 * og; e += 64) {
+      const int tap = e / (16 * og), c = 16 * gown + e % (16 * og);
+      bslice[e] = c < a.d ? a.base[size_t(tap) * a.d + c] : 0.f;
+    }
+  }
+  // ---- every MMA of this CTA is done: the operand ring is free ----
+  if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+  tc_fence_after();
+  const int quarter = warp & 3;
+  // [orows][pitch]: this CTA's groups (all 128 rows when S = 1), past the
+  // warps' transpose blocks
+  float* corr = reinterpret_cast<float*>(smem + kPScratch);
+  if (S == 1) {
+    // TMEM lane = W_c row = tap * 64 + group, column = position: all rows are ours
+    const int row = quarter * 32 + lane;
+    for (int c = warp < 4 ? 32 : 0; c < Np; c += 64) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c + 4 * q < Np)
+          *reinterpret_cast<float4*>(corr + size_t(row) * pitch + c + 4 * q) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+  } else {
+    // The partial tile [128 W_c rows][Np] goes to this split's slice of the
+    // workspace, except the rows of the groups this CTA mixes, which stay in
+    // corr.  Each 32 x 32 block passes through the warp's scratch (16-byte
+    // chunks XOR-swizzled by row), so that a store instruction writes four rows
+    // of 128 contiguous bytes.
+    float* part = a.ws + (size_t(tile) * S + split) * (size_t(2 * kPGroups) * Np);
+    float4* blk = reinterpret_cast<float4*>(smem) + warp * 256;
+    const int q = lane & 7;
+    for (int c = warp < 4 ? 32 : 0; c < Np; c += 64) {
+      float v[32];
+      tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        blk[lane * 8 + (k ^ (lane & 7))] =
+            make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      __syncwarp();
+      if (c + 4 * q < Np) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int rr = 4 * k + (lane >> 3);  // row of the block
+          const int row = quarter * 32 + rr, gl = row % kPGroups;
+          const float4 f = blk[rr * 8 + (q ^ (rr & 7))];
+          if (gl / og == split)
+            *reinterpret_cast<float4*>(corr + size_t((row / kPGroups) * og + gl % og) * pitch + c +
+                                       4 * q) = f;
+          else
+            __stcg(reinterpret_cast<float4*>(part + size_t(row) * Np + c + 4 * q), f);
+        }
+      }
+      __syncwarp();
+    }
+  }
+  tc_fence_before();
+  // every slice of the cluster is written (release / acquire at cluster scope)
+  if (S > 1) cluster_sync_all(); else __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  pdl_launch_dependents();
+  if (S > 1) {
+    // ---- this CTA's rows (tap j, group split*og + i) summed over the S slices
+    // in rank order, read through L2; two items per thread at a time so that
+    // 2*S loads are in flight ----
+    const float* parts = a.ws + size_t(tile) * S * (size_t(2 * kPGroups) * Np);
+    const size_t slice = size_t(2 * kPGroups) * Np;
+    const int n4 = orows * (Np / 4);
+    for (int e0 = tid; e0 < n4; e0 += 2 * kCThreads) {
+      float4 v[2][kCMaxSplits];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = min(e0 + h * kCThreads, n4 - 1);
+        const int orow = e / (Np / 4), c4 = e % (Np / 4);
+        const int row = (orow / og) * kPGroups + split * og + orow % og;
+        const float* src = parts + size_t(row) * Np + 4 * c4;
+#pragma unroll
+        for (int k = 0; k < kCMaxSplits; ++k)
+          if (k < S)
+            v[h][k] = k == split
+                          ? *reinterpret_cast<const float4*>(corr + size_t(orow) * pitch + 4 * c4)
+                          : __ldcg(reinterpret_cast<const float4*>(src + k * slice));
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * kCThreads;
+        if (e >= n4) break;
+        float4 acc = v[h][0];
+#pragma unroll
+        for (int k = 1; k < kCMaxSplits; ++k)
+          if (k < S) {
+            acc.x += v[h][k].x; acc.y += v[h][k].y; acc.z += v[h][k].z; acc.w += v[h][k].w;
+          }
+        const int orow = e / (Np / 4), c4 = e % (Np / 4);
+        *reinterpret_cast<float4*>(corr + size_t(orow) * pitch + 4 * c4) = acc;
+      }
+    }
+    __syncthreads();
+  }
+  // ---- the 2-tap mix: item = (group, 8 channels, run of kPRun positions) ----
+  const int np = min(Np, a.R - p0);
+  const int ncolumn = 2 * og;
+  const int items = ncolumn * ((np + kPRun - 1) / kPRun);
+  for (int item = tid; item < items; item += kCThreads) {
+    const int col = item % ncolumn, i0 = (item / ncolumn) * kPRun;
+    const int gl = col >> 1, h = col & 1, g = gown + gl;
+    if (g >= a.G) continue;
+    const int ch0 = 16 * g + 8 * h;
+    const int pf = p0 + i0;  // the run's first position
+    uint4 cur[kPRun];
+#pragma unroll
+    for (int u = 0; u < kPRun; ++u)
+      if (i0 + u < np)
+        cur[u] = *reinterpret_cast<const uint4*>(a.x + size_t(pf + u) * a.d + ch0);
+    uint4 prev = *reinterpret_cast<const uint4*>(
+        (pf % a.L == 0 ? a.x_prev + size_t(pf / a.L) * a.d : a.x + size_t(pf - 1) * a.d) + ch0);
+    float b0[8], b1[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      b0[j] = bslice[16 * gl + 8 * h + j];
+      b1[j] = bslice[16 * og + 16 * gl + 8 * h + j];
+    }
+    const float* c0p = corr + size_t(gl) * pitch + i0;
+    const float* c1p = corr + size_t(og + gl) * pitch + i0;
+#pragma unroll
+    for (int u = 0; u < kPRun; ++u) {
+      if (i0 + u >= np) break;
+      const int pp = pf + u;
+      if (u > 0 && pp % a.L == 0)  // a sequence starts inside the run
+        prev = *reinterpret_cast<const uint4*>(a.x_prev + size_t(pp / a.L) * a.d + ch0);
+      const float c0 = c0p[u], c1 = c1p[u];
+      float xt[8], xm[8];
+      bf8_unpack(cur[u], xt);
+      bf8_unpack(prev, xm);
+      uint32_t ow[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float lo = fmaf(b0[2 * q] + c0, xt[2 * q], (b1[2 * q] + c1) * xm[2 * q]);
+        const float hi =
+            fmaf(b0[2 * q + 1] + c0, xt[2 * q + 1], (b1[2 * q + 1] + c1) * xm[2 * q + 1]);
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
+        ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
+      }
+      *reinterpret_cast<uint4*>(a.y + size_t(pp) * a.d + ch0) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+      prev = cur[u];
+    }
+  }
+}
+
+bool g_conv_ptile_attr[64];
+
+// Tile width and split for the position-tiled kernel: tiles of 256 positions
+// (one CTA per SM) or 128 (two per SM), each with the largest power-of-two
+// cluster (<= 8) whose CTAs all fit on the SMs at once; of the two, the one
+// whose busiest SM moves the fewest bytes (operand ring, its partial tile out
+// and the other splits' slices of its rows back, the mix).  (Tiles of 224
+// positions, 120 CTAs at 1,024 positions x d = 2560, measured 14.9 us per
+// call against 13.9 for 256, and 128-position tiles in clusters of 4 14.6:
+// the partial stores slow down with more writers.  The runtime's count of
+// resident clusters of 8 at this shared-memory size is below the 12 that were
+// measured to start together, so it is not used.)
+// The kernel runs only with a split (splits > 1); otherwise conv_tc_kernel runs.
+struct PtilePlan {
+  int Np, splits, kps, stages, tiles;
+  size_t smem, ws_bytes;
+  long long cost;
+};
+PtilePlan ptile_plan(int R, int G, int kblocks, int sms) {
+  PtilePlan best{};
+  best.cost = -1;
+  for (const int want : {256, 128}) {
+    const int Np = std::min(want, (R + 15) / 16 * 16);
+    const int stages = Np > 128 ? kPMaxStages : 3;
+    const size_t smem = ptile_smem_bytes(Np, stages);
+    const long long slots = (long long)sms * (smem <= size_t(113) * 1024 ? 2 : 1);
+    const long long tiles = (long long)((R + Np - 1) / Np) * ((G + kPGroups - 1) / kPGroups);
+    int S = 1;
+    while (S * 2 <= kCMaxSplits && tiles * S * 2 <= slots && S * 2 <= kblocks) S *= 2;
+    int kps = (kblocks + S - 1) / S;
+    while (S > 1 && (S - 1) * kps >= kblocks) {  // keep every split non-empty
+      S >>= 1;
+      kps = (kblocks + S - 1) / S;
+    }
+    const long long busiest = (tiles * S + sms - 1) / sms;
+    const long long per_cta = (long long)kps * ptile_stage_bytes(Np) +
+                              2LL * (S - 1) * (2 * kPGroups / S) * Np * 4 +
+                              (long long)(kPGroups / S) * 16 * Np * 4;
+    const long long cost = busiest * per_cta;
+    if (tiles * S <= slots && (best.cost < 0 || cost < best.cost))
+      best = PtilePlan{Np, S, kps, stages, static_cast<int>(tiles), smem,
+                       ptile_ws_bytes(tiles, S, Np), cost};
+  }
+  return best;
+}
+// Measured (20 chained calls): at 1,024 positions x d = 2560 the split kernel
+// (256-position tiles) took 13.9 us per call against 17.4 for conv_tc_kernel;
+// at 128 positions (24 CTAs) 10.6 against 8.4.  So it runs only when its CTAs
+// fill half the GPU in one wave of clusters.
+bool use_ptile(int R, int d, const PtilePlan& pl, int sms) {
+  return R > kSMaxRows && d % kCBK == 0 && d / kGroup >= kPGroups / 2 && pl.splits > 1 &&
+         2LL * pl.tiles * pl.splits >= sms;
+}
+
+// ============================================================================
 // At most 16 positions (batch 1): one correction group mixed per CTA.
 // ============================================================================
 // A cluster of C CTAs owns C consecutive correction groups.  CTA `rank` copies
@@ -850,9 +1197,16 @@ cudaError_t launch_gemv_c(const ConvGemvArgs& a, cudaStream_t s, int dev) {
 
 }  // namespace
 
+size_t conv2_ws_bytes(int B, int L, int d) {
+  const int R = B * L;
+  const int sms = device_info().sms;
+  const PtilePlan pl = ptile_plan(R, d / kGroup, d / kCBK, sms);
+  return use_ptile(R, d, pl, sms) ? pl.ws_bytes : 0;
+}
+
 cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, const float* base,
                          const __nv_bfloat16* W_c, int B, int L, int d, __nv_bfloat16* y,
-                         cudaStream_t s) {
+                         void* ws, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -905,6 +1259,40 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
       return cudaErrorInvalidValue;
     return launch_kc(conv_small_kernel, dim3(tiles * c.splits), dim3(kCThreads),
                      small_smem_bytes(c.Npad, c.splits), s, true, c.splits, c, tmW);
+  }
+  const PtilePlan pl = ws ? ptile_plan(R, d / kGroup, d / kCBK, sms) : PtilePlan{};
+  if (ws && use_ptile(R, d, pl, sms)) {
+    // ---- many positions: position tiles x 64 groups, K split over a cluster ----
+    if (!g_conv_ptile_attr[dev & 63]) {
+      e = cudaFuncSetAttribute(conv_ptile_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kCSmemMax));
+      if (e != cudaSuccess) return e;
+      g_conv_ptile_attr[dev & 63] = true;
+    }
+    ConvPtileArgs c{};
+    c.x = x;
+    c.x_prev = x_prev;
+    c.base = base;
+    c.y = y;
+    c.R = R;
+    c.L = L;
+    c.d = d;
+    c.G = d / kGroup;
+    c.kblocks = d / kCBK;
+    c.ws = static_cast<float*>(ws);
+    c.Np = pl.Np;
+    c.gtiles = (c.G + kPGroups - 1) / kPGroups;
+    c.splits = pl.splits;
+    c.kps = pl.kps;
+    c.stages = pl.stages;
+    c.err = device_error_word();
+    const int tiles = pl.tiles;
+    alignas(64) CUtensorMap tmW, tmX;
+    if (!tensor_map_bf16(W_c, uint64_t(2) * c.G, uint64_t(d), kPGroups, &tmW) ||
+        !tensor_map_bf16(x, uint64_t(R), uint64_t(d), static_cast<uint32_t>(c.Np), &tmX))
+      return cudaErrorInvalidValue;
+    return launch_kc(conv_ptile_kernel, dim3(tiles * c.splits), dim3(kCThreads), pl.smem, s, true,
+                     c.splits, c, tmW, tmX);
   }
   ConvArgs a{};
   a.x = x;

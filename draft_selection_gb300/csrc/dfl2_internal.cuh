@@ -256,9 +256,12 @@ cudaError_t launch_walk(const float* scores, const int32_t* cand_idx, int B, int
                         float* q, cudaStream_t s, bool pdl);
 
 // ---- conv ---------------------------------------------------------------------
+// ws: NULL, or conv2_ws_bytes(B, L, d) bytes of device memory (the position-
+// tiled split-K kernel exchanges its partial tiles there).
+size_t conv2_ws_bytes(int B, int L, int d);
 cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, const float* base,
                          const __nv_bfloat16* W_c, int B, int L, int d, __nv_bfloat16* y,
-                         cudaStream_t s);
+                         void* ws, cudaStream_t s);
 
 // ---- LM head + top-16 (lmhead.cu) ---------------------------------------------
 struct LmheadPlan {

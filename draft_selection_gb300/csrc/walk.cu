@@ -6,9 +6,9 @@
 // step t from row i of S_t depends only on that row and on step t's draw (the
 // Philox counter is t, not the path).  So one CTA per sequence stages the
 // sequence's L x 16 x 16 score table in shared memory, takes the decision of
-// every row in parallel (walk_row_choice16, 16 lanes per row: greedy argmax or
-// the Philox draw from softmax(S/T)), and one thread then follows the chosen
-// slots from the verified token: L dependent shared-memory reads.
+// every row in parallel (walk_row_choice: greedy argmax or the Philox draw from
+// softmax(S/T)), and one thread then follows the chosen slots from the verified
+// token: L dependent shared-memory reads.
 #include "dfl2_internal.cuh"
 
 namespace dfl2 {
@@ -44,23 +44,14 @@ __global__ void __launch_bounds__(kWalkThreads) walk_kernel(WalkArgs a) {
   }
   __syncthreads();
   const uint64_t seed = a.T > 0.f ? a.seeds[b] : 0ull;
-  // 16 lanes per row, 16 rows per pass; every lane takes part in every pass
-  // (the decision is a half-warp collective), rows past the table included
-  const int j = tid & 15;
-  for (int r0 = 0; r0 < L * kCand; r0 += kWalkThreads / 16) {
-    const int r = r0 + tid / 16;
-    const bool real = r < L * kCand;
-    const int t = real ? r / kCand : 0, i = r % kCand;
-    const float u = a.T > 0.f ? walk_uniform(seed, a.cycle, t) : 0.f;
-    float q_j;
-    const int c = walk_row_choice16(real ? tab[size_t(r) * kCand + j] : 0.f, a.T, u, q_j);
-    if (!real) continue;
+  for (int r = tid; r < L * kCand; r += kWalkThreads) {
+    const int t = r / kCand, i = r % kCand;
     if (t == 0 && i > 0) {  // position 0 has only the verified token's row
-      if (j == 0) choice[r] = 0;
+      choice[r] = 0;
       continue;
     }
-    tab[size_t(r) * kCand + j] = q_j;
-    if (j == 0) choice[r] = c;
+    const float u = a.T > 0.f ? walk_uniform(seed, a.cycle, t) : 0.f;
+    choice[r] = walk_row_choice(tab + size_t(r) * kCand, a.T, u, tab + size_t(r) * kCand);
   }
   __syncthreads();
   if (tid == 0) {

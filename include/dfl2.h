@@ -196,6 +196,27 @@ dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* b
                        const uint16_t* W_c, int B, int L, int d, uint16_t* y,
                        dfl2_stream stream);
 
+/* The same conv with a workspace.  With many positions (B*L > 64, d a multiple
+ * of 64 and at least 512) the correction product is split over K across a
+ * thread-block cluster and the partial products are exchanged through the
+ * workspace, which lets the call spread over the whole GPU; otherwise the
+ * call is the same as dfl2_conv2.  y is the same as dfl2_conv2's up to the
+ * order of the float32 additions (each partial sum is added in a fixed
+ * order, so a given shape always gives the same bits).
+ * dfl2_conv2_workspace_size: bytes of device memory the call needs for this
+ * shape on the current device (0: none, ws may be NULL); 0 also for an
+ * unsupported shape or when no device is usable.
+ * ws: device memory owned by the caller, at least that many bytes, not
+ * overlapping x or y; its contents are scratch (no state is kept between
+ * calls), and two calls that may run at the same time need separate
+ * workspaces.  Errors: DFL2_ERR_WORKSPACE if ws is NULL or ws_bytes is too
+ * small when bytes are needed; the argument errors of dfl2_conv2.
+ */
+size_t dfl2_conv2_workspace_size(int B, int L, int d);
+dfl2_status dfl2_conv2_ws(const uint16_t* x, const uint16_t* x_prev, const float* base,
+                          const uint16_t* W_c, int B, int L, int d, uint16_t* y, void* ws,
+                          size_t ws_bytes, dfl2_stream stream);
+
 /* ------------------------------------------------------------------ fused tail
  * top-16 -> pair scores -> walk in one call on one stream, with no host
  * synchronisation: the same results as dfl2_topk, dfl2_select and dfl2_walk
