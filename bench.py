@@ -42,7 +42,7 @@ NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
     ("topk", "serving_b64"): 314433792,     # topk16_kernel_serving_b64.md
     ("conv", "drafter4b_l16"): 1759744,     # conv_gemv_drafter4b_l16.md
-    ("conv", "serving_b64"): None,          # split-K conv not captured yet
+    ("conv", "serving_b64"): 7295744,       # conv_ptile_serving_b64.md
     ("lmhead", "drafter4b_l16"): 781673728,  # lmhead_topk_kernel_drafter4b_l16.md
     ("lmhead", "serving_b64"): 786832384,    # lmhead_topk_kernel_serving_b64.md
 }
@@ -185,9 +185,13 @@ class Case:
         self.dfl2.dfl2_tail(self.logits, i["verified"], i["hidden"], i["E"], i["W_A"], i["W_B"],
                             i["W_H"], self.T, self.seeds, 0, self.tokens, self.ws, q=self.q)
 
-    def conv(self, k=0):
+    def conv(self, k=0, plain=False):
+        """One conv call through dfl2_conv2_ws (plain: dfl2_conv2, no workspace)."""
         c = self.convs[k]
-        self.dfl2.dfl2_conv2_ws(c["x"], c["x_prev"], c["base"], c["W_c"], c["y"], self.conv_ws)
+        if plain:
+            self.dfl2.dfl2_conv2(c["x"], c["x_prev"], c["base"], c["W_c"], c["y"])
+        else:
+            self.dfl2.dfl2_conv2_ws(c["x"], c["x_prev"], c["base"], c["W_c"], c["y"], self.conv_ws)
 
     def convs20(self):
         for k in range(len(self.convs)):
@@ -564,7 +568,8 @@ def profile_op(args) -> int:
         fn = lambda: dfl2.dfl2_lmhead_topk(lm["hidden"], lm["W_lm"], lm_idx, lm_val, lm_ws)
     else:
         fn = {"topk": case.topk, "select": case.select, "walk": case.walk,
-              "conv": lambda: case.conv(0), "tail": case.tail, "step": case.step}[args.profile_op]
+              "conv": lambda: case.conv(0), "conv_plain": lambda: case.conv(0, plain=True),
+              "tail": case.tail, "step": case.step}[args.profile_op]
     for _ in range(args.steps):
         fn()
     torch.cuda.synchronize()
@@ -585,7 +590,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--profile-op",
-                    choices=["topk", "select", "walk", "conv", "tail", "step", "lmhead"],
+                    choices=["topk", "select", "walk", "conv", "conv_plain", "tail", "step",
+                             "lmhead"],
                     help="run one op --steps times, untimed, for a profiler; no JSON line")
     args = ap.parse_args()
     if args.profile_op:
