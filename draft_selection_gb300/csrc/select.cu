@@ -58,6 +58,7 @@ struct GemmArgs {
   GemmProblem prob[3];
   int tiles_before[3];  // tiles of the problems before this one
   int splits, kps, kblocks;  // splits = cluster size along K
+  int nsplit;                // CTAs per row tile along N: 1 (256 columns) or 2 (128 each)
   const __nv_bfloat16* E;
   const __nv_bfloat16* hidden;
   const int32_t* cand_idx;  // [B,L,16]
@@ -102,9 +103,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // CTA -> (m tile, split); the splits of one tile form one cluster
+  // CTA -> (m tile, column part, split); the splits of one (tile, part) form one cluster
   const int split = blockIdx.x % a.splits;
-  const int rem = blockIdx.x / a.splits;
+  const int rem = (blockIdx.x / a.splits) / a.nsplit;
+  const int bn = kBN / a.nsplit;                                   // output columns of this CTA
+  const int n0 = ((blockIdx.x / a.splits) % a.nsplit) * bn;        // the first of them
   const int p = rem >= a.tiles_before[2] ? 2 : (rem >= a.tiles_before[1] ? 1 : 0);
   const GemmProblem& P = a.prob[p];
   const int m0 = (rem - a.tiles_before[p]) * kBM;
@@ -126,8 +129,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // (the top-16) still runs: a prefetch into L2 is coherent with writes in
   // flight, so it may precede the dependency wait.
   // One CTA per K range (the problem's first row tile) asks for it.
-  if (P.W && nkb > 0 && m0 == 0)
-    prefetch_l2_rows(P.W + size_t(tid) * a.d + size_t(kb0) * kBK, uint32_t(nkb) * kBK * 2u);
+  if (P.W && nkb > 0 && m0 == 0 && tid < bn)
+    prefetch_l2_rows(P.W + size_t(n0 + tid) * a.d + size_t(kb0) * kBK, uint32_t(nkb) * kBK * 2u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -146,8 +149,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         record_error(a.err, kDevErrGemm);
       const int kelem = (kb0 + it) * kBK;
       if (tid == 0) {
-        mbar_arrive_expect_tx(&full_bar[s], kBStage);
-        tma_load_2d(sB + size_t(s) * kBStage, tmap, kelem, 0, &full_bar[s]);
+        mbar_arrive_expect_tx(&full_bar[s], uint32_t(bn) * kBK * 2u);
+        tma_load_2d(sB + size_t(s) * kBStage, tmap, kelem, n0, &full_bar[s]);
       }
       uint8_t* dstA = sA + size_t(s) * kAStage;
 #pragma unroll
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {
     if (warp == 4 && lane == 0) {
       // ---- MMA issuer ----
-      constexpr uint32_t idesc = umma_idesc_bf16(kBM, kBN);
+      const uint32_t idesc = umma_idesc_bf16(kBM, bn);
       for (int it = 0; it < nkb; ++it) {
         const int s = it % kGStages;
         if (!mbar_wait(&full_bar[s], (it / kGStages) & 1)) record_error(a.err, kDevErrGemm);
@@ -192,11 +195,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int quarter = warp & 3;
       const int row = m0 + quarter * 32 + lane;
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < bn / 32; ++c) {
         float v[32];
         tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
         if (row < P.M) {
-          float4* o = reinterpret_cast<float4*>(P.out + size_t(row) * kBN + c * 32);
+          float4* o = reinterpret_cast<float4*>(P.out + size_t(row) * kBN + n0 + c * 32);
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
@@ -230,7 +233,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int lrow = quarter * 32 + lane;
 #pragma unroll 1
-    for (int c = 0; c < kBN / 32; ++c) {
+    for (int c = 0; c < bn / 32; ++c) {
       float v[32];
       tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(c * 32), v);
       float4* o = reinterpret_cast<float4*>(stage + size_t(lrow) * kStagePitch + c * 32);
@@ -242,9 +245,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   {
     const int rows = max(0, min(kBM, P.M - m0));
-    for (int e = tid; e < rows * (kBN / 4); e += kGemmThreads) {
-      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
-      *reinterpret_cast<float4*>(mypart + size_t(m0 + lr) * kBN + 4 * c4) =
+    for (int e = tid; e < rows * (bn / 4); e += kGemmThreads) {
+      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      *reinterpret_cast<float4*>(mypart + size_t(m0 + lr) * kBN + n0 + 4 * c4) =
           *reinterpret_cast<const float4*>(stage + size_t(lr) * kStagePitch + 4 * c4);
     }
   }
@@ -259,7 +262,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int per = (kBM + S - 1) / S;
   const int r0 = split * per;
   const int valid_rows = max(0, min(min(per, kBM - r0), P.M - (m0 + r0)));
-  const int n4 = valid_rows * (kBN / 4);
+  const int n4 = valid_rows * (bn / 4);
   constexpr int kMaxSplitLoads = kMaxClusterSplits;
   constexpr int kPer = 2;  // elements per thread and pass: 2 x 8 loads in flight
   for (int e0 = tid; e0 < n4; e0 += kGemmThreads * kPer) {
@@ -267,8 +270,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int e = e0 + u * kGemmThreads;
-      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
-      const size_t at = size_t(m0 + r0 + lr) * kBN + 4 * c4;
+      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      const size_t at = size_t(m0 + r0 + lr) * kBN + n0 + 4 * c4;
 #pragma unroll
       for (int k = 0; k < kMaxSplitLoads; ++k)  // every split's value requested first
         v[u][k] = k < S && e < n4
@@ -279,13 +282,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = 0; u < kPer; ++u) {
       const int e = e0 + u * kGemmThreads;
       if (e >= n4) break;
-      const int lr = e / (kBN / 4), c4 = e % (kBN / 4);
+      const int lr = e / (bn / 4), c4 = e % (bn / 4);
       float4 acc = v[u][0];
 #pragma unroll
       for (int k = 1; k < kMaxSplitLoads; ++k) {  // rank order: deterministic
         acc.x += v[u][k].x; acc.y += v[u][k].y; acc.z += v[u][k].z; acc.w += v[u][k].w;
       }
-      *reinterpret_cast<float4*>(P.out + size_t(m0 + r0 + lr) * kBN + 4 * c4) = acc;
+      *reinterpret_cast<float4*>(P.out + size_t(m0 + r0 + lr) * kBN + n0 + 4 * c4) = acc;
     }
   }
 }
@@ -777,6 +780,10 @@ SelectPlan select_plan(int B, int L, int d) {
     splits *= 2;
   p.kps = (p.kblocks + splits - 1) / splits;
   p.splits = (p.kblocks + p.kps - 1) / p.kps;  // every split gets at least one K block
+  // Still room for twice the CTAs (batch 1: 5 row tiles x 8 splits): each row
+  // tile's 256 outputs go to two CTAs of 128, which halves the W bytes and the
+  // partial tile of each CTA.
+  p.nsplit = tiles * p.splits * 2 <= kGemmTargetCtas ? 2 : 1;
   p.PA_off = 256;
   p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
   p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);
@@ -841,6 +848,7 @@ static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, 
     before += g.prob[i].mtiles;
   }
   g.splits = splits;
+  g.nsplit = 1;
   g.kps = kps;
   g.kblocks = d / kBK;
   g.E = E;
@@ -872,8 +880,9 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     g_gemm_attr[dev & 63] = true;
   }
   alignas(64) CUtensorMap tA, tB, tH;
-  if (!tensor_map_bf16(W_A, kRank, p.d, kBN, &tA) || !tensor_map_bf16(W_B, kRank, p.d, kBN, &tB) ||
-      !tensor_map_bf16(W_H, kRank, p.d, kBN, &tH))
+  const uint32_t bn = static_cast<uint32_t>(kBN / p.nsplit);
+  if (!tensor_map_bf16(W_A, kRank, p.d, bn, &tA) || !tensor_map_bf16(W_B, kRank, p.d, bn, &tB) ||
+      !tensor_map_bf16(W_H, kRank, p.d, bn, &tH))
     return cudaErrorInvalidValue;
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* PA = reinterpret_cast<float*>(w + p.PA_off);
@@ -897,6 +906,7 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     before += g.prob[i].mtiles;
   }
   g.splits = p.splits;
+  g.nsplit = p.nsplit;
   g.kps = p.kps;
   g.kblocks = p.kblocks;
   g.E = E;
@@ -907,8 +917,8 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   g.V = V;
   g.d = p.d;
   g.err = device_error_word();
-  e = launch_kc(proj_tc_kernel, dim3(before * p.splits), dim3(kGemmThreads), kGemmSmem, s, pdl,
-                p.splits, g, tA, tB, tH);
+  e = launch_kc(proj_tc_kernel, dim3(before * p.nsplit * p.splits), dim3(kGemmThreads), kGemmSmem,
+                s, pdl, p.splits, g, tA, tB, tH);
   if (e != cudaSuccess) return e;
   PairArgs qa{};
   qa.PA = PA;
