@@ -209,7 +209,7 @@ struct SelectPlan {
   int M;               // MA (kept for reporting)
   int kblocks;         // d / 64
   int kps, splits;     // K blocks per split; K splits = CTAs of one cluster (reduced on chip)
-  int nsplit;          // CTAs per row tile along the 256 outputs (1, or 2 of 128 columns)
+  int nsplit;          // CTAs per row tile along the 256 outputs (1, 2 or 4)
   size_t PA_off;       // float32 [MA][256]
   size_t PB_off;       // float32 [MB][256]
   size_t GH_off;       // float32 [MH][256], before the sigmoid

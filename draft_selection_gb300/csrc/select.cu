@@ -58,7 +58,7 @@ struct GemmArgs {
   GemmProblem prob[3];
   int tiles_before[3];  // tiles of the problems before this one
   int splits, kps, kblocks;  // splits = cluster size along K
-  int nsplit;                // CTAs per row tile along N: 1 (256 columns) or 2 (128 each)
+  int nsplit;                // CTAs per row tile along N: 1, 2 or 4 (256 / nsplit columns each)
   const __nv_bfloat16* E;
   const __nv_bfloat16* hidden;
   const int32_t* cand_idx;  // [B,L,16]
@@ -780,10 +780,11 @@ SelectPlan select_plan(int B, int L, int d) {
     splits *= 2;
   p.kps = (p.kblocks + splits - 1) / splits;
   p.splits = (p.kblocks + p.kps - 1) / p.kps;  // every split gets at least one K block
-  // Still room for twice the CTAs (batch 1: 5 row tiles x 8 splits): each row
-  // tile's 256 outputs go to two CTAs of 128, which halves the W bytes and the
-  // partial tile of each CTA.
-  p.nsplit = tiles * p.splits * 2 <= kGemmTargetCtas ? 2 : 1;
+  // While there is room for twice the CTAs (batch 1: 5 row tiles x 8 splits),
+  // each row tile's 256 outputs go to two (or four) CTAs, which divides the W
+  // bytes and the partial tile of each CTA.
+  p.nsplit = 1;
+  while (p.nsplit < 4 && tiles * p.splits * p.nsplit * 2 <= kGemmTargetCtas) p.nsplit *= 2;
   p.PA_off = 256;
   p.PB_off = align_up(p.PA_off + size_t(p.MA) * kRank * 4, 256);
   p.GH_off = align_up(p.PB_off + size_t(p.MB) * kRank * 4, 256);
