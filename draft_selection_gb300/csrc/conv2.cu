@@ -749,10 +749,10 @@ __global__ void __launch_bounds__(kCThreads, 2)
     }
   } else {
     // The partial tile [128 W_c rows][Np] goes to this split's slice of the
-    // workspace, except the rows of the groups this CTA mixes, which stay in
-    // corr.  Each 32 x 32 block passes through the warp's scratch (16-byte
-    // chunks XOR-swizzled by row), so that a store instruction writes four rows
-    // of 128 contiguous bytes.
+    // workspace (all of it: keeping the CTA's own rows in shared memory instead
+    // measured about 1 us slower per call).  Each 32 x 32 block passes through
+    // the warp's scratch (16-byte chunks XOR-swizzled by row), so that a store
+    // instruction writes four rows of 128 contiguous bytes.
     float* part = a.ws + (size_t(tile) * S + split) * (size_t(2 * kPGroups) * Np);
     float4* blk = reinterpret_cast<float4*>(smem) + warp * 256;
     const int q = lane & 7;
@@ -768,13 +768,8 @@ __global__ void __launch_bounds__(kCThreads, 2)
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const int rr = 4 * k + (lane >> 3);  // row of the block
-          const int row = quarter * 32 + rr, gl = row % kPGroups;
-          const float4 f = blk[rr * 8 + (q ^ (rr & 7))];
-          if (gl / og == split)
-            *reinterpret_cast<float4*>(corr + size_t((row / kPGroups) * og + gl % og) * pitch + c +
-                                       4 * q) = f;
-          else
-            __stcg(reinterpret_cast<float4*>(part + size_t(row) * Np + c + 4 * q), f);
+          __stcg(reinterpret_cast<float4*>(part + size_t(quarter * 32 + rr) * Np + c + 4 * q),
+                 blk[rr * 8 + (q ^ (rr & 7))]);
         }
       }
       __syncwarp();
@@ -806,9 +801,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
 #pragma unroll
         for (int k = 0; k < kCMaxSplits; ++k)
           if (k < S)
-            v[h][k] = k == split
-                          ? *reinterpret_cast<const float4*>(corr + size_t(orow) * pitch + 4 * c4)
-                          : __ldcg(reinterpret_cast<const float4*>(src + k * slice));
+            v[h][k] = __ldcg(reinterpret_cast<const float4*>(src + k * slice));
       }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
