@@ -31,7 +31,8 @@ def lib():
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
-    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_tail", "dfl2_verify",
+    for n in ("dfl2_topk", "dfl2_select", "dfl2_walk", "dfl2_conv2", "dfl2_conv2_ws",
+              "dfl2_conv2_workspace_size", "dfl2_tail", "dfl2_verify",
               "dfl2_tables_build", "dfl2_select_tables", "dfl2_tail_tables", "dfl2_lmhead_topk"):
         assert n in names
 
@@ -151,6 +152,20 @@ def test_conv_rejects_bad_arguments(lib):
     assert f(A, A2, A, A, 1, 8, 1024, A + 16, None) == INVALID                # y overlaps x
     assert "overlaps" in dfl2.dfl2_last_error()
     assert f(A, A2, A, A, 1, 0, 1024, A2 + 0x100000, None) == INVALID         # L = 0
+
+
+def test_conv_ws_rejects_bad_arguments(lib):
+    # the same host checks as dfl2_conv2, ahead of any workspace or CUDA call
+    f = lib.dfl2_conv2_ws
+    y = A2 + 0x100000
+    assert f(A, A2, A, A, 64, 16, 1000, y, A2 + 0x400000, 1 << 24, None) == UNSUPPORTED  # d % 16
+    assert f(None, A2, A, A, 64, 16, 2560, y, A2 + 0x400000, 1 << 24, None) == INVALID   # NULL x
+    assert f(A, A2, A, A, 64, 16, 2560, A + 16, A2 + 0x400000, 1 << 24, None) == INVALID  # y on x
+    assert "overlaps" in dfl2.dfl2_last_error()
+    assert f(A, A2, A, A, 0, 16, 2560, y, A2 + 0x400000, 1 << 24, None) == INVALID      # B = 0
+    # unsupported shapes need no workspace
+    assert dfl2.dfl2_conv2_workspace_size(0, 16, 2560) == 0
+    assert dfl2.dfl2_conv2_workspace_size(64, 16, 1000) == 0
 
 
 def test_tail_rejects_bad_arguments(lib):
