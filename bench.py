@@ -42,7 +42,7 @@ NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
     ("topk", "serving_b64"): 314433792,     # topk16_kernel_serving_b64.md
     ("conv", "drafter4b_l16"): 1759744,     # conv_gemv_drafter4b_l16.md
-    ("conv", "serving_b64"): 7295744,       # conv_ptile_serving_b64.md
+    ("conv", "serving_b64"): None,          # conv_ptile_serving_b64.md: an earlier variant
     ("lmhead", "drafter4b_l16"): 781673728,  # lmhead_topk_kernel_drafter4b_l16.md
     ("lmhead", "serving_b64"): 786832384,    # lmhead_topk_kernel_serving_b64.md
 }
