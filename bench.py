@@ -35,16 +35,16 @@ BATCHED = "serving_b64"
 METRIC = "µs per draft block at B=1; blocks/s and HBM GB/s vs roofline at B=64"
 FLUSH_BYTES = 256 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of the op's
-# kernel from the ncu captures summarised under profiles/, by (op, workload).  An
-# entry is removed when its kernel changes; ops without one report null.
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of an op's
+# kernel, by (op, workload), from one ncu capture of the kernel as it is now;
+# an op whose kernel changed since its capture has no entry and reports null.
 NCU_TRAFFIC = {
-    ("topk", "drafter4b_l16"): 4939520,     # topk16_rows_drafter4b_l16.md
-    ("topk", "serving_b64"): 314433792,     # topk16_kernel_serving_b64.md
-    ("conv", "drafter4b_l16"): 1759744,     # conv_gemv_drafter4b_l16.md
-    ("conv", "serving_b64"): None,          # conv_ptile_serving_b64.md: an earlier variant
-    ("lmhead", "drafter4b_l16"): 781673728,  # lmhead_topk_kernel_drafter4b_l16.md
-    ("lmhead", "serving_b64"): 786832384,    # lmhead_topk_kernel_serving_b64.md
+    ("topk", "drafter4b_l16"): 4939520,
+    ("topk", "serving_b64"): 314433792,
+    ("conv", "drafter4b_l16"): 1759744,
+    ("conv", "serving_b64"): 7291136,
+    ("lmhead", "drafter4b_l16"): 781673728,
+    ("lmhead", "serving_b64"): 786832384,
 }
 
 
@@ -148,30 +148,66 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+class Staged:
+    """Tensors packed into one device buffer (each slice 256-byte aligned), so
+    that a step's inputs (or outputs) move between host and device in one copy."""
+
+    def __init__(self, tensors, device):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += (t.numel() * t.element_size() + 255) // 256 * 256
+        self.buf = torch.empty(max(n, 256), dtype=torch.uint8, device=device)
+        self.views = []
+        for t, o in zip(tensors, offs):
+            nb = t.numel() * t.element_size()
+            v = self.buf[o:o + nb].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            self.views.append(v)
+        self.nbytes = n
+
+
 class Case:
-    """One workload resident on the device, with its step as callables."""
+    """One workload resident on the device, with its step as callables.  The
+    step's inputs that change every step (logits, hidden states, verified
+    tokens, Philox keys, and each conv call's x and x_prev) sit in one staging
+    buffer, and its outputs (tokens, q) in another."""
 
     def __init__(self, w: wl.Workload, T: float, device):
         import draft_selection_gb300 as dfl2
         self.dfl2 = dfl2
         self.w, self.T = w, T
         gen_dev = "cpu" if w.B == 1 else device
-        self.logits = wl.make_logits(w, gen_dev).to(device)
+        logits = wl.make_logits(w, gen_dev).to(device)
         inp = wl.make_tail_inputs(w, gen_dev)
         self.inp = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-        self.seeds = torch.from_numpy(inp["seeds"].view(np.int64)).to(device)
+        seeds = torch.from_numpy(inp["seeds"].view(np.int64)).to(device)
         self.convs = []
         for k in range(w.conv_calls):
             c = wl.make_conv_inputs(w, k, gen_dev)
             c = {n: t.to(device) for n, t in c.items()}
-            c["y"] = torch.empty_like(c["x"])
             self.convs.append(c)
+        per_step = [logits, self.inp["hidden"], self.inp["verified"], seeds]
+        for c in self.convs:
+            per_step += [c["x"], c["x_prev"]]
+        self.staged_in = Staged(per_step, device)
+        v = iter(self.staged_in.views)
+        self.logits, self.inp["hidden"], self.inp["verified"], self.seeds = (
+            next(v), next(v), next(v), next(v))
+        for c in self.convs:
+            c["x"], c["x_prev"] = next(v), next(v)
+            c["y"] = torch.empty_like(c["x"])
+        del per_step, logits
         # one conv workspace serves the block's calls: they run one after another
         n = dfl2.dfl2_conv2_workspace_size(w.B, w.L, w.d)
         self.conv_ws = dfl2.workspace(n, device) if n else None
         B, L = w.B, w.L
-        self.tokens = torch.empty(B, L, dtype=torch.int32, device=device)
-        self.q = torch.empty(B, L, 16, dtype=torch.float32, device=device) if T > 0 else None
+        outs = [torch.empty(B, L, dtype=torch.int32, device=device)]
+        if T > 0:
+            outs.append(torch.empty(B, L, 16, dtype=torch.float32, device=device))
+        self.staged_out = Staged(outs, device)
+        self.tokens = self.staged_out.views[0]
+        self.q = self.staged_out.views[1] if T > 0 else None
         self.ws = dfl2.workspace(dfl2.dfl2_tail_workspace_size(B, L, w.V, w.d), device)
         self.idx = torch.empty(B, L, 16, dtype=torch.int32, device=device)
         self.val = torch.empty(B, L, 16, dtype=torch.float32, device=device)
@@ -267,6 +303,38 @@ def time_graph(g, steps, warmup, flush):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def graph_floor(steps, warmup, flush):
+    """Device time of a graph replay holding one trivial kernel (a 4-byte fill),
+    timed like the ops: the launch and event overhead inside every per-op number."""
+    tiny = torch.zeros(1, dtype=torch.int32, device=flush.device)
+    g, _ = capture(lambda: tiny.fill_(1))
+    return summarize(time_graph(g, steps, warmup, flush))
+
+
+def sustained(g, seconds):
+    """Mean device time per replay of g run back to back (no flush, no host gap)
+    for about `seconds`: the steady state, and load for the clock sampler."""
+    stream = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    b.synchronize()
+    per = max(a.elapsed_time(b), 1e-3)
+    n = max(10, int(seconds * 1e3 / per))
+    done, total_ms = 0, 0.0
+    while done < n:
+        k = min(n - done, 2000)
+        a.record(stream)
+        for _ in range(k):
+            g.replay()
+        b.record(stream)
+        b.synchronize()
+        total_ms += a.elapsed_time(b)
+        done += k
+    return total_ms / done
+
+
 def summarize(ts):
     return {"mean_ms": float(np.mean(ts)), "median_ms": float(np.median(ts)),
             "min_ms": float(np.min(ts))}
@@ -305,6 +373,7 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
     # back to back (one graph launch amortised over them), per call.
     c20 = summarize(time_graph(g_c20, sub, warmup, flush))
     res["conv"] = {k: v / w.conv_calls for k, v in c20.items()}
+    res["floor"] = graph_floor(sub, warmup, flush)
     res["kernels_per_step"] = k_step
     build_ms = case.build_tables()
     g_tt, _ = capture(case.tail_tables)
@@ -417,16 +486,13 @@ def measure_lmhead(w: wl.Workload, device, steps, warmup, flush, pk):
 
 
 def measure_e2e(case: Case, g_step, steps, warmup, flush):
-    """The same step with the inputs copied from pinned host memory and the
-    result read back inside the timed region."""
-    host_in = [case.logits, case.inp["hidden"], case.inp["verified"], case.seeds]
-    for c in case.convs:
-        host_in += [c["x"], c["x_prev"]]
-    pinned = [t.detach().cpu().pin_memory() for t in host_in]
-    out_dev = [case.tokens] + ([case.q] if case.q is not None else [])
-    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out_dev]
-    h2d = sum(t.numel() * t.element_size() for t in pinned)
-    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    """The same step with its inputs copied from pinned host memory (one copy of
+    the staging buffer) and its outputs read back (one copy) inside the timed
+    region."""
+    pinned_in = case.staged_in.buf.detach().cpu().pin_memory()
+    pinned_out = torch.empty(case.staged_out.buf.shape, dtype=torch.uint8, pin_memory=True)
+    h2d = case.staged_in.nbytes
+    d2h = case.staged_out.nbytes
     stream = torch.cuda.current_stream()
     ts = []
     for i in range(warmup + steps):
@@ -434,11 +500,9 @@ def measure_e2e(case: Case, g_step, steps, warmup, flush):
         torch.cuda._sleep(20000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for dst, src in zip(host_in, pinned):
-            dst.copy_(src, non_blocking=True)
+        case.staged_in.buf.copy_(pinned_in, non_blocking=True)
         g_step.replay()
-        for dst, src in zip(out_host, out_dev):
-            dst.copy_(src, non_blocking=True)
+        pinned_out.copy_(case.staged_out.buf, non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= warmup:
@@ -589,6 +653,8 @@ def main():
     ap.add_argument("--batched", default=BATCHED, help="second workload ('' to skip)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps after the timed region")
     ap.add_argument("--profile-op",
                     choices=["topk", "select", "walk", "conv", "conv_plain", "tail", "step",
                              "lmhead"],
@@ -619,6 +685,9 @@ def main():
     barrier(world)
     res, g_step = measure_native(case, args.steps, args.warmup, flush, pk, which)
     step_ms = max_over_ranks(res["step"]["mean_ms"], world)
+    # the step back to back for a few seconds: steady state with warm L2 and the
+    # GPU under load while the clocks are sampled
+    sustained_ms = sustained(g_step, args.sustain_s)
     barrier(world)
     e2e_ms, h2d, d2h = measure_e2e(case, g_step, max(3, min(args.steps, 200)), args.warmup, flush)
     e2e_ms = max_over_ranks(e2e_ms, world)
@@ -675,6 +744,13 @@ def main():
             "conv20_us": round(res["conv"]["mean_ms"] * 1e3 * w.conv_calls, 2),
             "kernel_us": {k: round(res[k]["mean_ms"] * 1e3, 2) for k in
                           ("topk", "select", "walk", "conv", "conv_alone")},
+            # per-op graphs minus the one-kernel graph floor (launch + events),
+            # comparable with ncu's per-launch durations; conv is already per
+            # call of a 20-call graph, so it keeps its value
+            "graph_floor_us": round(res["floor"]["mean_ms"] * 1e3, 2),
+            "kernel_us_net": {k: round((res[k]["mean_ms"] - res["floor"]["mean_ms"]) * 1e3, 2)
+                              for k in ("topk", "select", "walk", "tail", "conv_alone")},
+            "sustained_step_us": round(sustained_ms * 1e3, 2),
             "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
             "per_kernel": res["per_kernel"],
             "tables": res["tables"],

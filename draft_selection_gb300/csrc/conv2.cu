@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
     if (lane == 0) {  // ---- producer: x rows and both taps' W_c rows by TMA ----
       const uint32_t tx = static_cast<uint32_t>(kCAStage + bst);
       for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
-        if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrConv);
+        if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrConv);
         const int kb = kb0 + it;
         const int k0 = kb * kCBK;
         const int keep = kb - kbk0;  // in [0, side): this x tile stays for the mix
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
     if (lane == 0) {  // ---- MMA issuer ----
       const uint32_t idesc = umma_idesc_bf16(kCBM, N);
       for (int it = 0, s = 0, ph = 0; it < nkb; ++it) {
-        if (!mbar_wait(&full_bar[s], ph)) record_error(a.err, kDevErrConv);
+        if (!mbar_wait(&full_bar[s], ph, a.err)) record_error(a.err, kDevErrConv);
         tc_fence_after();
         const int keep = kb0 + it - kbk0;
         const uint64_t ad = umma_desc_sw128(keep >= 0 && keep < a.side ? sKeep + size_t(keep) * kCAStage
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(kCThreads) conv_tc_kernel(const __grid_constan
     // into the receive slot of the CTA that owns them (split K).  The accumulator
     // is complete only when every MMA, and so every read of the stages, is done. ----
     const int quarter = warp & 3;
-    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+    if (!mbar_wait(accum_bar, 0, a.err)) record_error(a.err, kDevErrConv);
     tc_fence_after();
     const int lrow = quarter * 32 + lane;
     const int per = (kCBM + a.splits - 1) / a.splits;
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     // ---- producer: W_c rows by TMA (two boxes of 64 rows), x rows by cp.async ----
     for (int it = 0; it < nkb; ++it) {
       const int st = it % kSStages;
-      if (it >= kSStages && !mbar_wait(&empty_bar[st], ((it / kSStages) - 1) & 1))
+      if (it >= kSStages && !mbar_wait(&empty_bar[st], ((it / kSStages) - 1) & 1, a.err))
         record_error(a.err, kDevErrConv);
       const int k0 = (kb0 + it) * kCBK;
       uint8_t* dA = sA + size_t(st) * kCAStage;
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
       const uint32_t idesc = umma_idesc_bf16(kCBM, Np);
       for (int it = 0; it < nkb; ++it) {
         const int st = it % kSStages;
-        if (!mbar_wait(&full_bar[st], (it / kSStages) & 1)) record_error(a.err, kDevErrConv);
+        if (!mbar_wait(&full_bar[st], (it / kSStages) & 1, a.err)) record_error(a.err, kDevErrConv);
         tc_fence_after();
         const uint64_t ad = umma_desc_sw128(sA + size_t(st) * kCAStage);
         const uint64_t bd = umma_desc_sw128(sB + size_t(st) * Np * 128);
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
   } else {
     // ---- TMEM row r = W_c row (tap r/64, group g0 + r%64), columns = positions:
     // push the R values to the CTA that mixes that group ----
-    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+    if (!mbar_wait(accum_bar, 0, a.err)) record_error(a.err, kDevErrConv);
     tc_fence_after();
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
@@ -693,7 +693,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
       const uint32_t tx = static_cast<uint32_t>(sbytes);
       for (int it = 0; it < nkb; ++it) {
         const int st = it % nst;
-        if (it >= nst && !mbar_wait(&empty_bar[st], ((it / nst) - 1) & 1))
+        if (it >= nst && !mbar_wait(&empty_bar[st], ((it / nst) - 1) & 1, a.err))
           record_error(a.err, kDevErrConv);
         const int k0 = (kb0 + it) * kCBK;
         uint8_t* dst = ring + size_t(st) * sbytes;
@@ -709,7 +709,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
       const uint32_t idesc = umma_idesc_bf16(kCBM, Np);
       for (int it = 0; it < nkb; ++it) {
         const int st = it % nst;
-        if (!mbar_wait(&full_bar[st], (it / nst) & 1)) record_error(a.err, kDevErrConv);
+        if (!mbar_wait(&full_bar[st], (it / nst) & 1, a.err)) record_error(a.err, kDevErrConv);
         tc_fence_after();
         const uint64_t ad = umma_desc_sw128(ring + size_t(st) * sbytes);
         const uint64_t bd = umma_desc_sw128(ring + size_t(st) * sbytes + kCAStage);
@@ -729,7 +729,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
     }
   }
   // ---- every MMA of this CTA is done: the operand ring is free ----
-  if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrConv);
+  if (!mbar_wait(accum_bar, 0, a.err)) record_error(a.err, kDevErrConv);
   tc_fence_after();
   const int quarter = warp & 3;
   // [orows][pitch]: this CTA's groups (all 128 rows when S = 1), past the
@@ -1093,7 +1093,7 @@ __global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArg
     const uint32_t bbase = smem_u32(wsm + size_t(bvalid ? rb : 0) * pitch + 2 * bcol);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     if (s0 < s1) {
-      if (!mbar_wait(&bar[st], 0)) record_error(a.err, kDevErrConv);
+      if (!mbar_wait(&bar[st], 0, a.err)) record_error(a.err, kDevErrConv);
       for (int k = s0; k < s1; ++k) {
         uint32_t af[4], bfr[2];
         ldsm_x4(abase + 32u * k, af);
@@ -1127,7 +1127,7 @@ __global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArg
   if constexpr (C == 1) __syncthreads();
   if (!mixer) return;
   if constexpr (C > 1) {
-    if (!mbar_wait_cluster(&bar[2], 0)) record_error(a.err, kDevErrConv);
+    if (!mbar_wait_cluster(&bar[2], 0, a.err)) record_error(a.err, kDevErrConv);
   }
   // ---- the 2-tap mix of 8 channels at position p ----
   const int pm = tid >> 1;

@@ -25,6 +25,11 @@ enum DeviceError : uint32_t {
 
 // About two seconds at the GB300's maximum SM clock: far beyond any legitimate wait.
 constexpr long long kWaitCycles = 4000000000LL;
+// A wait that has lasted this long (about half a millisecond) also gives up as
+// soon as any kernel has recorded an error in the device's error word: once one
+// wait of a launch has run out, the launch's other waits end within about
+// kGiveUpCycles each instead of kWaitCycles.
+constexpr long long kGiveUpCycles = 1LL << 20;
 
 __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code) {
   if (err) atomicCAS(err, 0u, code);
@@ -61,12 +66,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase: false when kWaitCycles pass without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// True when a wait that started at t0 must give up: kWaitCycles have passed,
+// or kGiveUpCycles have and the error word `err` (nullable) is set.
+__device__ __forceinline__ bool wait_expired(long long t0, const uint32_t* err) {
+  const long long dt = clock64() - t0;
+  if (dt > kWaitCycles) return true;
+  return err && dt > kGiveUpCycles && *reinterpret_cast<const volatile uint32_t*>(err) != 0u;
+}
+// Bounded wait on a phase: false when it expires (wait_expired) first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const uint32_t* err = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (wait_expired(t0, err)) return false;
   }
   return true;
 }
@@ -91,7 +104,8 @@ __device__ __forceinline__ void mbar_arrive_remote(const uint64_t* bar, uint32_t
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a) : "memory");
 }
 // Bounded wait (acquire at cluster scope) on a local barrier that other CTAs arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const uint32_t* err = nullptr) {
   const long long t0 = clock64();
   while (true) {
     uint32_t ok;
@@ -103,7 +117,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     if (ok) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (wait_expired(t0, err)) return false;
   }
 }
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -132,12 +146,13 @@ __device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
   asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
   return v;
 }
-// Bounded wait until *p > n; false on timeout.
-__device__ __forceinline__ bool wait_count_above(const uint32_t* p, uint32_t n) {
+// Bounded wait until *p > n; false when it expires (wait_expired) first.
+__device__ __forceinline__ bool wait_count_above(const uint32_t* p, uint32_t n,
+                                                 const uint32_t* err = nullptr) {
   if (ld_acquire_cta(p) > n) return true;
   const long long t0 = clock64();
   while (ld_acquire_cta(p) <= n) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (wait_expired(t0, err)) return false;
   }
   return true;
 }

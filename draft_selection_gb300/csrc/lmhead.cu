@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       for (int i = 0; i < nt && ok; ++i) {
         const int n0 = (t_lo + i) * kLBN;
         for (int kb = 0; kb < a.kblocks; ++kb, ++it) {
-          if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1)) {
+          if (it >= nst && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) {
             record_error(a.err, kDevErrGemm);
             ok = false;
             break;
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       // the last (up to nst) copies issued: their phases complete when they land
       for (int back = 1; back <= nst && back <= it; ++back) {
         const int j = it - back;
-        mbar_wait(&full_bar[j % nst], (j / nst) & 1);
+        mbar_wait(&full_bar[j % nst], (j / nst) & 1, a.err);
       }
     }
     __syncwarp();
@@ -250,14 +250,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
       bool ok = true;
       for (int i = 0; i < nt && ok; ++i) {
         const int b = i & 1;
-        if (i >= 2 && !mbar_wait(&acce_bar[b], ((i >> 1) - 1) & 1)) {
+        if (i >= 2 && !mbar_wait(&acce_bar[b], ((i >> 1) - 1) & 1, a.err)) {
           record_error(a.err, kDevErrGemm);
           break;
         }
         tc_fence_after();
         const uint32_t acc = tmem + static_cast<uint32_t>(b * kLBN);
         for (int kb = 0; kb < a.kblocks; ++kb) {
-          if (!mbar_wait(&full_bar[s], ph)) {
+          if (!mbar_wait(&full_bar[s], ph, a.err)) {
             record_error(a.err, kDevErrGemm);
             ok = false;
             break;
@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       }
       // every MMA this thread issued has completed before TMEM is freed
       umma_commit(done_bar);
-      mbar_wait(done_bar, 0);
+      mbar_wait(done_bar, 0, a.err);
     }
     __syncwarp();
   } else {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     for (int i = 0; i < nt; ++i) {
       const int b = i & 1;
       // warp-uniform outcome: the TMEM loads below are warp-collective
-      if (!__all_sync(kAll, mbar_wait(&accf_bar[b], (i >> 1) & 1))) {
+      if (!__all_sync(kAll, mbar_wait(&accf_bar[b], (i >> 1) & 1, a.err))) {
         record_error(a.err, kDevErrGemm);
         break;
       }

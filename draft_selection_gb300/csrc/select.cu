@@ -12,15 +12,20 @@
 // (128-byte swizzle); the gathered rows by 16-byte cp.async written in the same
 // swizzle; the accumulator lives in TMEM (256 columns).  When there are too few
 // tiles to fill the GPU (batch 1), K is split over the CTAs of a thread-block
-// cluster: each CTA parks its fp32 partial tile in its own shared memory and
-// every CTA sums one slice of rows across the cluster through distributed
-// shared memory, in rank order, so the result is deterministic and no partial
-// ever reaches HBM.
+// cluster: each CTA stages its fp32 partial tile in shared memory and stores it
+// to the caller's workspace in whole rows (the partials stay in L2), one
+// cluster barrier, then every CTA sums one slice of rows over the splits in
+// rank order, so the result is deterministic.
 //
-// Stage 2, the pair kernel: one CTA per (sequence, position) forms the 16x16
-// scores from the previous position's A rows, the gate and this position's B
-// rows (2x2 register blocking over 16-byte shared-memory reads).  In the fused tail it also takes the walk's decision for each of its
-// 16 rows, and the last CTA of each sequence follows the chosen slots.
+// Stage 2, the pair scores: a position's 16x16 scores from the previous
+// position's A rows, the gate and this position's B rows (2x2 register
+// blocking over 16-byte shared-memory reads).  In the fused tail
+// (pair_walk_kernel, L <= 32) one thread-block cluster serves each sequence:
+// each position takes the walk's decision for every predecessor row and hands
+// the choices to the cluster's first CTA through distributed shared memory,
+// which follows the chosen slots.  dfl2_select (scores only) and blocks longer
+// than 32 positions use pair16_kernel, one CTA per (sequence, position); with
+// the walk fused, the last CTA of each sequence (ticket) follows the slots.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = 0; i < 8; ++i) src[i] = a_row(a, P.kind, m0 + (tid >> 3) + 16 * i, P.M);
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kGStages;
-      if (it >= kGStages && !mbar_wait(&empty_bar[s], ((it / kGStages) - 1) & 1))
+      if (it >= kGStages && !mbar_wait(&empty_bar[s], ((it / kGStages) - 1) & 1, a.err))
         record_error(a.err, kDevErrGemm);
       const int kelem = (kb0 + it) * kBK;
       if (tid == 0) {
@@ -176,7 +181,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const uint32_t idesc = umma_idesc_bf16(kBM, bn);
       for (int it = 0; it < nkb; ++it) {
         const int s = it % kGStages;
-        if (!mbar_wait(&full_bar[s], (it / kGStages) & 1)) record_error(a.err, kDevErrGemm);
+        if (!mbar_wait(&full_bar[s], (it / kGStages) & 1, a.err)) record_error(a.err, kDevErrGemm);
         tc_fence_after();
         const uint64_t ad = umma_desc_sw128(sA + size_t(s) * kAStage);
         const uint64_t bd = umma_desc_sw128(sB + size_t(s) * kBStage);
@@ -188,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       umma_commit(accum_bar);
     }
     __syncwarp();
-    if (!mbar_wait(accum_bar, 0)) record_error(a.err, kDevErrGemm);
+    if (!mbar_wait(accum_bar, 0, a.err)) record_error(a.err, kDevErrGemm);
     tc_fence_after();
     if (a.splits == 1) {
       // ---- one split: TMEM -> registers -> the output rows ----
@@ -702,7 +707,7 @@ __global__ void __launch_bounds__(kPairThreads * P) pair_walk_kernel(PairArgs a)
   if (rank != 0) return;
   // ---- first CTA: follow the chosen slots from the verified token ----
   if (threadIdx.x == 0) {
-    if (CL > 1 && !mbar_wait_cluster(&w->bar, 0)) record_error(a.err, kDevErrGemm);
+    if (CL > 1 && !mbar_wait_cluster(&w->bar, 0, a.err)) record_error(a.err, kDevErrGemm);
     int prev = 0;
     for (int tt = 0; tt < a.L; ++tt) {
       prev = w->choice[tt][prev] & (kCand - 1);

@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
       int t = static_cast<int>(g0 - row * tpr);
       const int n = static_cast<int>(g1 - g0);
       for (int i = 0, s = 0, ph = 0; i < n; ++i) {
-        if (i >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrTopkEmpty);
+        if (i >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
         const size_t off = size_t(t) * kTileBytes;
         const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
         mbar_arrive_expect_tx(&full_bar[s], bytes);
@@ -451,8 +451,8 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
     const int jw = ((warp - i0) % kConsumerWarps + kConsumerWarps) % kConsumerWarps;
     auto tile_of = [&](int j, const uint4*& tile, int& nvec, uint32_t& elem_base) {
       const int i = i0 + j, st = i % kStages;
-      if (!wait_count_above(issued, static_cast<uint32_t>(i)) ||
-          !mbar_wait(&full_bar[st], (i / kStages) & 1))
+      if (!wait_count_above(issued, static_cast<uint32_t>(i), a.err) ||
+          !mbar_wait(&full_bar[st], (i / kStages) & 1, a.err))
         record_error(a.err, kDevErrTopkFull);
       const int t = t0 + j;
       nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
@@ -798,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   if (warp == kConsumerWarps) {  // producer
     if (lane == 0) {
       for (int i = 0, s = 0, ph = 0; i < n; ++i) {
-        if (i >= kRStages && !mbar_wait(&empty_bar[s], ph ^ 1)) record_error(a.err, kDevErrTopkEmpty);
+        if (i >= kRStages && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
         const size_t off = size_t(t_lo + i) * kTileBytes;
         const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
         mbar_arrive_expect_tx(&full_bar[s], bytes);
@@ -816,8 +816,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
     // Warp w scans tiles w, w + 8, ...: each stage serves one warp only.
     auto stage_of = [&](int i, const uint4*& tile, int& nvec, uint32_t& eb) {
       const int st = i % kRStages;
-      if (!wait_count_above(issued, static_cast<uint32_t>(i)) ||
-          !mbar_wait(&full_bar[st], (i / kRStages) & 1))
+      if (!wait_count_above(issued, static_cast<uint32_t>(i), a.err) ||
+          !mbar_wait(&full_bar[st], (i / kRStages) & 1, a.err))
         record_error(a.err, kDevErrTopkFull);
       const int t = t_lo + i;
       nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
@@ -908,7 +908,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
     }
   }
   if (rank == 0 && warp < kConsumerWarps) {
-    if (C > 1 && !mbar_wait_cluster(list_bar, 0)) record_error(a.err, kDevErrTopkFull);
+    if (C > 1 && !mbar_wait_cluster(list_bar, 0, a.err)) record_error(a.err, kDevErrTopkFull);
     named_sync(1, kConsumers);  // the first CTA's own list is in place too
     if (threadIdx.x < kCand) res[threadIdx.x] = 0ull;
     named_sync(1, kConsumers);

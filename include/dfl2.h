@@ -42,9 +42,13 @@
  *     multiple of 64 for dfl2_select and of 16 for dfl2_conv2; V >= 16, L >= 1,
  *     B >= 1.  Logits rows must be a whole number of 16-byte units (V % 8 == 0
  *     for bf16, V % 4 == 0 for float32).
- *   - Every wait inside a kernel is bounded; a wait that runs out records a
- *     code in a per-device error word (dfl2_device_error) and the kernel
- *     returns, leaving the context usable.
+ *   - Every wait inside a kernel is bounded.  A wait that runs out (about 2 s
+ *     of SM clock) records a code in a per-device error word
+ *     (dfl2_device_error) and the kernel carries on without the data it
+ *     waited for, so that launch's outputs are undefined; it still ends and
+ *     leaves the context usable.  Once the error word is set, every other wait
+ *     that has lasted about 0.5 ms gives up too, so a launch whose pipeline
+ *     stalls ends within a few seconds, not one full timeout per wait.
  *   - Workspaces must be zero-filled once before their first use (for example
  *     with dfl2_workspace_init); the library keeps them valid afterwards.
  */

@@ -72,8 +72,8 @@ def test_small_workloads(name, e_std):
            bilinear_mean_abs=float(np.nanmean(np.where(np.isinf(ref), np.nan, bil))))
 
 
-@pytest.mark.parametrize("name,nseq", [("serving_b64", 3), ("stress_b256_ties", 2)])
-def test_batched_workloads_sampled(name, nseq):
+@pytest.mark.parametrize("name,nseq", [("serving_b64", 64), ("stress_b256_ties", 32)])
+def test_batched_workloads(name, nseq):
     w = wl.WORKLOADS[name]
     inp = wl.make_tail_inputs(w, "cuda")
     lg = wl.make_logits(w, "cuda")
@@ -83,10 +83,12 @@ def test_batched_workloads_sampled(name, nseq):
     idx = idx.int().contiguous()
     val = val.contiguous()
     S = gpu_select(idx, val, inp["verified"], inp)
-    seqs = sorted({0, w.B - 1} | set(np.random.default_rng(3).choice(w.B, nseq, False).tolist()))
+    # every sequence, or nseq spread evenly over the batch (every row tile and wave)
+    seqs = (list(range(w.B)) if nseq >= w.B else
+            sorted({int(round(i * (w.B - 1) / (nseq - 1))) for i in range(nseq)}))
     ref = oracle_select_subset(idx.cpu(), val.cpu(), inp["verified"].cpu(), inp, seqs)
     worst = assert_scores_close(S[seqs], ref, name)
-    report(kind="scores", what=f"{name} sampled {seqs}", worst_err_over_tol=worst)
+    report(kind="scores", what=f"{name} {len(seqs)} of {w.B} sequences", worst_err_over_tol=worst)
 
 
 @pytest.mark.parametrize("B,L", [(1, 1), (3, 2), (5, 17)])

@@ -84,14 +84,22 @@ def test_small_workloads(name, T, e_std):
     check_tail(w, lg, inp, T, inp["seeds"], 0, list(range(w.B)))
 
 
-@pytest.mark.parametrize("name,T,nseq", [("serving_b64", 1.0, 3), ("stress_b256_ties", 0.0, 2),
-                                         ("stress_b256_ties", 0.7, 2)])
-def test_batched_workloads_sampled(name, T, nseq):
+def batched_seqs(w, nseq):
+    """Every sequence when nseq >= B; otherwise nseq sequences spread evenly over
+    the batch (first and last included), so that the checked rows fall in every
+    row tile and every wave of the projection GEMM."""
+    if nseq >= w.B:
+        return list(range(w.B))
+    return sorted({int(round(i * (w.B - 1) / (nseq - 1))) for i in range(nseq)})
+
+
+@pytest.mark.parametrize("name,T,nseq", [("serving_b64", 1.0, 64), ("stress_b256_ties", 0.0, 32),
+                                         ("stress_b256_ties", 0.7, 32)])
+def test_batched_workloads(name, T, nseq):
     w = wl.WORKLOADS[name]
     lg = wl.make_logits(w, "cuda")
     inp = wl.make_tail_inputs(w, "cuda")
-    seqs = sorted({0, w.B - 1} | set(np.random.default_rng(5).choice(w.B, nseq, False).tolist()))
-    check_tail(w, lg, inp, T, inp["seeds"], 12345, seqs)
+    check_tail(w, lg, inp, T, inp["seeds"], 12345, batched_seqs(w, nseq))
 
 
 def test_tail_equals_the_three_calls():

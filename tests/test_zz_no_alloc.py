@@ -41,19 +41,42 @@ def without_workspace(lg):
     return idx, val
 
 
-def test_matches_dfl2_topk_on_two_calls_in_a_row():
-    # Call 1: the batch-1 4B-drafter block (16 rows, each split across many CTAs,
-    # so the scratch tickets and partial lists are used).  Call 2: a different
-    # shape and dtype right after, on the same stream, reusing the same scratch.
-    first = wl.make_logits(wl.WORKLOADS["drafter4b_l16"], "cpu").cuda()
-    second = wl.make_logits(wl.WORKLOADS["tiny_l8_v32k"].with_(B=3, L=5), "cpu").cuda()
-    a1 = without_workspace(first)
-    a2 = without_workspace(second)
-    b1 = with_workspace(first)
-    b2 = with_workspace(second)
+def _persistent_split_path(B, L, V):
+    """True when dfl2_topk runs its persistent kernel for this shape, where rows
+    are split across CTAs and the partial lists and per-row tickets live in the
+    scratch: the cluster-per-row kernel (few rows) uses no scratch at all.  The
+    rule restates the library's dispatch: one cluster of C <= 8 CTAs per row
+    while rows * C <= 2 * SMs and each CTA streams at most 16 tiles of 8 KB."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    tiles = -(-V * 2 // 8192)  # bf16 rows
+    C = min(8, tiles)
+    while C > 1 and B * L * C > 2 * sms:
+        C //= 2
+    return not (B * L * C <= 2 * sms and -(-tiles // C) <= 16)
+
+
+def test_matches_dfl2_topk_on_calls_in_a_row():
+    # Two calls in a row on a shape whose rows are split across CTAs (the
+    # scratch's partial lists and tickets are used; the second call reuses the
+    # tickets the first one left), then a shape with four times the rows (a
+    # different ticket and partial-list layout in the same array), then the
+    # batch-1 4B-drafter block, which takes the scratch-free cluster kernel.
+    base = wl.WORKLOADS["serving_b64"]
+    split16 = base.with_(B=16)
+    split64 = base
+    for w in (split16, split64):
+        assert _persistent_split_path(w.B, w.L, w.V), w
+        assert dfl2.dfl2_topk_workspace_size(w.B, w.L, w.V) <= 4 << 20
+    first = wl.make_logits(split16, "cuda")
+    second = wl.make_logits(split64.with_(seed=2003), "cuda")
+    third = wl.make_logits(wl.WORKLOADS["drafter4b_l16"], "cpu").cuda()
+    got = [without_workspace(first), without_workspace(first), without_workspace(second),
+           without_workspace(third)]
+    want = [with_workspace(first), with_workspace(first), with_workspace(second),
+            with_workspace(third)]
     torch.cuda.synchronize()
     assert dfl2.dfl2_device_error() == 0
-    for (ia, va), (ib, vb) in ((a1, b1), (a2, b2)):
+    for (ia, va), (ib, vb) in zip(got, want):
         np.testing.assert_array_equal(ia.cpu().numpy(), ib.cpu().numpy())
         np.testing.assert_array_equal(va.cpu().numpy(), vb.cpu().numpy())
 
