@@ -924,26 +924,31 @@ bool use_ptile(int R, int d, const PtilePlan& pl, int sms) {
 }
 
 // ============================================================================
-// At most 16 positions (batch 1): one correction group mixed per CTA.
+// At most 16 positions (batch 1): K split over a cluster, groups mixed per CTA.
 // ============================================================================
-// A cluster of C CTAs owns C consecutive correction groups.  CTA `rank` copies
-// the K slice [rank*d/C, (rank+1)*d/C) of the cluster's 2C W_c rows and of
-// every position of x into shared memory (bulk copies, in two K halves with a
-// barrier each, so half the warps start on the first half while the second
-// lands), forms the R x 2C partial corrections with warp-level bf16 MMAs
-// (m16n8k16: the positions are M, the W_c rows N, float32 accumulators; each
-// warp a share of the K steps), adds the warps' partials and sends each
-// group's two rows to the CTA that mixes the group with st.async, which
-// counts the bytes on the receiver's mbarrier: no cluster-wide barrier at the
-// end.  The receiver sums the C slices in rank order and applies the 2-tap mix
-// to its 16 channels.  The contraction is 2 x R x d per group, far below a
-// tcgen05 tile (M >= 64), and the call is latency-bound, so the warp-level MMA
-// is the cheaper instrument here.
-// The kernel lets the next launch on the stream start at once and, before
-// waiting on the previous launch, prefetches its slices of W_c and x into L2 (a
-// prefetch into L2 is coherent with writes still in flight, so nothing stale is
-// read); every real read follows the dependency wait.
+// A cluster of C CTAs owns NG = C * MG consecutive correction groups, whose
+// 2 NG W_c rows (tap 0 then tap 1) form the N of a warp-level MMA.  CTA `rank`
+// holds the K slice [rank*d/C, (rank+1)*d/C) of those rows and of every
+// position of x; it forms the R x 2NG partial corrections with m16n8k16 bf16
+// MMAs (positions as M, float32 accumulators, each warp a share of the K
+// steps), adds the warps' partials and sends each group's rows to the CTA that
+// mixes the group with st.async, which counts the bytes on the receiver's
+// mbarrier: no cluster-wide barrier at the end.  The receiver sums the C
+// slices in rank order (deterministic) and applies the 2-tap mix to its MG
+// groups.  The contraction is 2 NG x R x d per cluster, far below a tcgen05
+// tile, and the call is latency-bound, so the warp-level MMA is the cheaper
+// instrument here.
+//
+// Latency: the kernel lets the next launch on the stream start at once, and
+// before waiting on the previous launch it copies its W_c slice into shared
+// memory and reads its base slice: these are weights, which no kernel still
+// pending on the stream writes (the documented contract of the conv entry
+// points), so the copy overlaps the previous kernel.  After the wait only x is
+// read: each warp copies just the 16-byte pieces of x its own K steps use
+// (cp.async), so no CTA-wide barrier sits between the wait and the MMAs; the
+// mixing threads load their x_t and x_{t-1} at the same time.
 constexpr int kGvThreads = 256;  // 8 warps
+constexpr int kGvWarps = kGvThreads / 32;
 constexpr int kGvMaxR = 16;      // positions = the MMA's 16 rows
 constexpr size_t kGvSmemMax = 200 * 1024;
 
@@ -957,11 +962,15 @@ struct ConvGemvArgs {
   uint32_t* err;
 };
 
+// Row pitch in bytes of the x and W_c slices: 16 more than the slice, so that
+// pitch / 16 is odd and the eight rows of an ldmatrix fall in distinct banks.
 __host__ __device__ constexpr int gemv_pitch(int d, int C) { return 2 * (d / C) + 16; }
-__host__ __device__ constexpr size_t gemv_smem_bytes(int d, int C) {
-  // [16 x rows | 2C W_c rows] (padded pitch) [warp partials 8 x 16 x 8 f32]
-  // [receive C x 2 x 16 f32] [3 mbarriers]
-  return size_t(16 + 2 * C) * gemv_pitch(d, C) + 8 * 16 * 8 * 4 + size_t(C) * 2 * 16 * 4 + 32;
+__host__ __device__ constexpr int gemv_rows(int C, int MG) { return 2 * C * MG; }
+// [16 x rows | max(NR, 8) W_c rows] [warp partials 8 x 16 x NR f32]
+// [receive C x 2 x MG x 16 f32] [2 mbarriers]
+__host__ __device__ constexpr size_t gemv_smem_bytes(int d, int C, int MG) {
+  return size_t(16 + (gemv_rows(C, MG) < 8 ? 8 : gemv_rows(C, MG))) * gemv_pitch(d, C) +
+         size_t(kGvWarps) * 16 * gemv_rows(C, MG) * 4 + size_t(C) * 2 * MG * 16 * 4 + 32;
 }
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
@@ -981,14 +990,15 @@ __device__ __forceinline__ void mma_16816_bf16(float d[4], const uint32_t a[4], 
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// 4-byte store into CTA `rank`'s shared memory, counted as transaction bytes on
-// that CTA's mbarrier at the same offset as `bar`.
-__device__ __forceinline__ void st_async_f32(const void* local, uint32_t rank, float v,
-                                             const uint64_t* bar) {
-  const uint32_t a = dsmem_addr(local, rank), b = dsmem_addr(bar, rank);
-  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(a),
-               "f"(v), "r"(b)
-               : "memory");
+// 16-byte store into CTA `rank`'s shared memory, counted as transaction bytes
+// on that CTA's mbarrier at the same offset as `bar`.
+__device__ __forceinline__ void st_async_v4(const void* local, uint32_t rank, float4 v,
+                                            const uint64_t* bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(dsmem_addr(local, rank)),
+      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(dsmem_addr(bar, rank))
+      : "memory");
 }
 __device__ __forceinline__ void bf8_to_f32(const uint4 v, float f[8]) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -999,143 +1009,152 @@ __device__ __forceinline__ void bf8_to_f32(const uint4 v, float f[8]) {
   }
 }
 
-template <int C>
+template <int C, int MG>
 __global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArgs a) {
-  constexpr int NR = 2 * C;  // W_c rows of the cluster, tap-major: row r = tap r/C, group r%C
-  static_assert(NR <= 8, "the W_c rows are the MMA's 8 columns");
+  constexpr int NG = C * MG;           // groups of the cluster
+  constexpr int NR = 2 * NG;           // their W_c rows: row n = tap * NG + group
+  constexpr int NT = (NR + 7) / 8;     // n8 tiles of the MMA
+  constexpr int NRS = NT * 8;          // W_c rows staged (rows past NR repeat row 0)
+  static_assert(NR <= 32, "the W_c rows are loaded by one warp");
   extern __shared__ __align__(128) uint8_t gsm[];
-  const int d = a.d, ks = d / C, pitch = gemv_pitch(d, C);
+  const int d = a.d, ks = d / C, pitch = gemv_pitch(d, C), R = a.R;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int rank = C > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int gc0 = (blockIdx.x / C) * C;  // first group of the cluster
-  const int gmix = gc0 + rank;           // the group this CTA mixes
+  const int gc0 = (blockIdx.x / C) * NG;  // first group of the cluster
   const int k0 = rank * ks;
-  uint8_t* xs = gsm;                                // [16][pitch]
-  uint8_t* wsm = gsm + size_t(16) * pitch;          // [NR][pitch]
-  float* red = reinterpret_cast<float*>(wsm + size_t(NR) * pitch);  // [8][16][8]
-  float* recv = red + 8 * 16 * 8;                   // [C][2][16]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(recv + C * 2 * 16);  // [0..1] K halves, [2] receive
-  // K halves: two stages when each half is a whole number of 16-wide steps
-  const int nst = (ks / 2) % 16 == 0 ? 2 : 1;
-  const int hk = ks / nst;  // elements per stage
+  uint8_t* xs = gsm;                                                // [16][pitch]
+  uint8_t* wsm = gsm + size_t(16) * pitch;                          // [NRS][pitch]
+  float* red = reinterpret_cast<float*>(wsm + size_t(NRS) * pitch);  // [8][16][NR]
+  float* recv = red + kGvWarps * 16 * NR;                           // [C][2][MG][16]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(recv + C * 2 * MG * 16);  // [0] W_c, [1] receive
+  const int nq = (R + 3) / 4;  // four-position pieces sent per W_c row
 
   pdl_launch_dependents();
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
-    mbar_init(&bar[2], 1);
     fence_mbar_init();
-    // every CTA of the cluster (this one included) sends 2 x R floats here
-    if (C > 1) mbar_arrive_expect_tx(&bar[2], uint32_t(C) * 2u * uint32_t(a.R) * 4u);
+    mbar_arrive_expect_tx(&bar[0], uint32_t(NR) * uint32_t(ks) * 2u);
+    // every CTA of the cluster (this one included) sends 2 MG rows of nq pieces here
+    if (C > 1) mbar_arrive_expect_tx(&bar[1], uint32_t(C * 2 * MG * nq * 16));
   }
-  if (tid < NR) {
-    const int g = gc0 + tid % C;
-    if (g < a.G) prefetch_l2(a.W_c + (size_t(tid / C) * a.G + g) * d + k0, uint32_t(ks) * 2u);
-  } else if (tid >= 32 && tid < 32 + a.R) {
-    prefetch_l2(a.x + size_t(tid - 32) * d + k0, uint32_t(ks) * 2u);
+  __syncthreads();  // the barriers are initialised before any copy completes on them
+  // ---- before the dependency wait: weights only ----
+  if (warp == 0 && lane < NR) {
+    const int tap = lane / NG, gi = lane % NG;
+    const int g = gc0 + gi < a.G ? gc0 + gi : 0;  // a missing group reads a real row (never stored)
+    bulk_g2s(wsm + size_t(lane) * pitch, a.W_c + (size_t(tap) * a.G + g) * d + k0,
+             uint32_t(ks) * 2u, &bar[0]);
+  } else if (warp == 1 && lane < R) {
+    // x may still be being written: an L2 prefetch is coherent with those writes
+    prefetch_l2(a.x + size_t(lane) * d + k0, uint32_t(ks) * 2u);
   }
-  if constexpr (C > 1) cluster_arrive_release();  // barrier inits visible to the peers
-  __syncthreads();
-  pdl_wait();
-
-  if (warp == 0) {
-    // lane i < R: x row i; lane 16 + r: W_c row r (both K halves, one barrier each)
-    if (lane == 0) {
-      int nw = 0;
-      for (int r = 0; r < NR; ++r) nw += gc0 + r % C < a.G;
-      for (int s = 0; s < nst; ++s)
-        mbar_arrive_expect_tx(&bar[s], uint32_t(a.R + nw) * uint32_t(hk) * 2u);
-    }
-    __syncwarp();
-    const __nv_bfloat16* src = nullptr;
-    uint8_t* dst = nullptr;
-    if (lane < a.R) {
-      src = a.x + size_t(lane) * d + k0;
-      dst = xs + size_t(lane) * pitch;
-    } else if (lane >= 16 && lane < 16 + NR && gc0 + (lane - 16) % C < a.G) {
-      const int r = lane - 16;
-      src = a.W_c + (size_t(r / C) * a.G + gc0 + r % C) * d + k0;
-      dst = wsm + size_t(r) * pitch;
-    }
-    if (src)
-      for (int s = 0; s < nst; ++s)
-        bulk_g2s(dst + size_t(s) * hk * 2, src + size_t(s) * hk, uint32_t(hk) * 2u, &bar[s]);
-  }
-  // ---- operands of the mix (one thread per position and half group), in flight early ----
-  const bool mixer = tid < 2 * a.R && gmix < a.G;
-  uint4 xt = make_uint4(0u, 0u, 0u, 0u), xm = xt;
+  // mixing threads: (group m of this CTA, position p, half of the 16 channels)
+  const int m_mix = tid / (2 * R), p_mix = (tid % (2 * R)) >> 1, h_mix = tid & 1;
+  const int gmix = gc0 + rank * MG + m_mix;
+  const bool mixer = tid < 2 * R * MG && gmix < a.G;
+  const int cmix = 16 * gmix + 8 * h_mix;
   float4 b0[2], b1[2];
   if (mixer) {
-    const int p = tid >> 1, c = 16 * gmix + 8 * (tid & 1);
-    const int t = p % a.L;
-    xt = __ldcg(reinterpret_cast<const uint4*>(a.x + size_t(p) * d + c));
-    xm = __ldcg(reinterpret_cast<const uint4*>(
-        (t > 0 ? a.x + size_t(p - 1) * d : a.x_prev + size_t(p / a.L) * d) + c));
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
-      b0[h] = __ldcg(reinterpret_cast<const float4*>(a.base + c) + h);
-      b1[h] = __ldcg(reinterpret_cast<const float4*>(a.base + d + c) + h);
+      b0[h] = __ldg(reinterpret_cast<const float4*>(a.base + cmix) + h);
+      b1[h] = __ldg(reinterpret_cast<const float4*>(a.base + d + cmix) + h);
     }
   }
-  // ---- partial corrections: acc = x_slice (16 x K) * W_slice^T (K x 8) over this warp's steps ----
-  {
-    const int st = nst == 2 ? warp >> 2 : 0;       // the K half this warp reads
-    const int wi = nst == 2 ? warp & 3 : warp;     // its index among that half's warps
-    const int nw = nst == 2 ? 4 : 8;
-    const int steps = hk / 16;
-    const int s0 = st * steps + wi * steps / nw, s1 = st * steps + (wi + 1) * steps / nw;
+  if constexpr (C > 1) cluster_arrive_release();  // barrier inits visible to the peers
+  pdl_wait();
+
+  // ---- the mix's operands, in flight during the MMAs ----
+  uint4 xt = make_uint4(0u, 0u, 0u, 0u), xm = xt;
+  if (mixer) {
+    const int t = p_mix % a.L;
+    xt = __ldcg(reinterpret_cast<const uint4*>(a.x + size_t(p_mix) * d + cmix));
+    xm = __ldcg(reinterpret_cast<const uint4*>(
+        (t > 0 ? a.x + size_t(p_mix - 1) * d : a.x_prev + size_t(p_mix / a.L) * d) + cmix));
+  }
+  // ---- partial corrections: this warp's K steps of x_slice (16 x K) * W_slice^T ----
+  const int steps = ks / 16;
+  const int s0 = warp * steps / kGvWarps, s1 = (warp + 1) * steps / kGvWarps;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+  if (s0 < s1) {
+    const int per_row = (s1 - s0) * 2;  // 16-byte pieces of one x row
+    for (int e = lane; e < R * per_row; e += 32) {
+      const int p = e / per_row, c = s0 * 16 + (e % per_row) * 8;
+      cp_async16(xs + size_t(p) * pitch + 2 * c, a.x + size_t(p) * d + k0 + c, true);
+    }
+    cp_async_commit();
     const int arow = lane & 15, acol = (lane >> 4) * 8;
     const int rb = lane & 7, bcol = ((lane >> 3) & 1) * 8;
-    const bool bvalid = rb < NR && gc0 + rb % C < a.G;
-    // rows past R and W_c rows past the cluster's valid groups read row 0: their
-    // products land in accumulator entries that are never used
-    const uint32_t abase = smem_u32(xs + size_t(arow < a.R ? arow : 0) * pitch + 2 * acol);
-    const uint32_t bbase = smem_u32(wsm + size_t(bvalid ? rb : 0) * pitch + 2 * bcol);
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (s0 < s1) {
-      if (!mbar_wait(&bar[st], 0, a.err)) record_error(a.err, kDevErrConv);
-      for (int k = s0; k < s1; ++k) {
-        uint32_t af[4], bfr[2];
-        ldsm_x4(abase + 32u * k, af);
-        ldsm_x2(bbase + 32u * k, bfr);
-        mma_16816_bf16(acc, af, bfr);
+    // rows past R read row 0: their products land in entries that are never sent
+    const uint32_t abase = smem_u32(xs + size_t(arow < R ? arow : 0) * pitch + 2 * acol);
+    if (!mbar_wait(&bar[0], 0, a.err)) record_error(a.err, kDevErrConv);
+    cp_async_wait<0>();
+    __syncwarp();
+#pragma unroll 1
+    for (int k = s0; k < s1; ++k) {
+      uint32_t af[4];
+      ldsm_x4(abase + 32u * k, af);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const int n = nt * 8 + rb;
+        uint32_t bfr[2];
+        ldsm_x2(smem_u32(wsm + size_t(n < NR ? n : 0) * pitch + 2 * bcol) + 32u * k, bfr);
+        mma_16816_bf16(acc[nt], af, bfr);
       }
     }
-    // acc: (position g, rows 2t, 2t+1), (position g+8, rows 2t, 2t+1)
+  }
+  {
+    // acc[nt]: (position g, rows nt*8 + 2t, +1), (position g + 8, the same rows)
     const int g = lane >> 2, t = lane & 3;
-    float* rw = red + warp * 128;
-    *reinterpret_cast<float2*>(rw + g * 8 + 2 * t) = make_float2(acc[0], acc[1]);
-    *reinterpret_cast<float2*>(rw + (g + 8) * 8 + 2 * t) = make_float2(acc[2], acc[3]);
+    float* rw = red + warp * 16 * NR;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int n = nt * 8 + 2 * t;
+      if (n < NR) {
+        *reinterpret_cast<float2*>(rw + g * NR + n) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(rw + (g + 8) * NR + n) = make_float2(acc[nt][2], acc[nt][3]);
+      }
+    }
   }
   if constexpr (C > 1) cluster_wait_acquire();  // the peers' barriers are initialised
   __syncthreads();
-  // ---- warp partials summed (warp order), row r sent to the CTA mixing group gc0 + r % C ----
-  if (tid < 16 * NR) {
-    const int p = tid / NR, r = tid % NR;
-    if (p < a.R) {
-      float v = 0.f;
+  // ---- warp partials summed (warp order); four positions of row n sent to the
+  // CTA that mixes group gc0 + n % NG ----
+  if (tid < nq * NR) {
+    const int n = tid % NR, q = tid / NR;
+    float v[4];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) v += red[w * 128 + p * 8 + r];
-      float* slot = recv + (rank * 2 + r / C) * 16 + p;
-      if constexpr (C > 1) {
-        if (gc0 + r % C < a.G) st_async_f32(slot, static_cast<uint32_t>(r % C), v, &bar[2]);
-      } else {
-        *slot = v;
-      }
+    for (int k = 0; k < 4; ++k) {
+      float s = 0.f;
+#pragma unroll
+      for (int w = 0; w < kGvWarps; ++w) s += red[(w * 16 + 4 * q + k) * NR + n];
+      v[k] = s;
     }
+    const int tap = n / NG, gi = n % NG;
+    float* slot = recv + ((rank * 2 + tap) * MG + gi % MG) * 16 + 4 * q;
+    const float4 val = make_float4(v[0], v[1], v[2], v[3]);
+    if constexpr (C > 1)
+      st_async_v4(slot, static_cast<uint32_t>(gi / MG), val, &bar[1]);
+    else
+      *reinterpret_cast<float4*>(slot) = val;
   }
-  if constexpr (C == 1) __syncthreads();
+  if constexpr (C == 1) {
+    __syncthreads();
+  } else {
+    // every CTA waits for its whole receive before it may exit (peers store into it)
+    if ((tid == 0 || mixer) && !mbar_wait_cluster(&bar[1], 0, a.err))
+      record_error(a.err, kDevErrConv);
+  }
   if (!mixer) return;
-  if constexpr (C > 1) {
-    if (!mbar_wait_cluster(&bar[2], 0, a.err)) record_error(a.err, kDevErrConv);
-  }
   // ---- the 2-tap mix of 8 channels at position p ----
-  const int pm = tid >> 1;
   float c0 = 0.f, c1 = 0.f;
 #pragma unroll
   for (int k = 0; k < C; ++k) {  // rank order: deterministic
-    c0 += recv[(k * 2 + 0) * 16 + pm];
-    c1 += recv[(k * 2 + 1) * 16 + pm];
+    c0 += recv[((k * 2 + 0) * MG + m_mix) * 16 + p_mix];
+    c1 += recv[((k * 2 + 1) * MG + m_mix) * 16 + p_mix];
   }
   float ft[8], fm[8];
   bf8_to_f32(xt, ft);
@@ -1151,42 +1170,46 @@ __global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArg
     const __nv_bfloat162 pr = __floats2bfloat162_rn(lo, hi);
     ow[q] = *reinterpret_cast<const uint32_t*>(&pr);
   }
-  *reinterpret_cast<uint4*>(a.y + size_t(pm) * d + 16 * gmix + 8 * (tid & 1)) =
-      make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  *reinterpret_cast<uint4*>(a.y + size_t(p_mix) * d + cmix) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
 }
 
-bool g_conv_gemv_attr[64][3];
+// (C, MG) instantiations and their attribute flags.
+constexpr int kGvShapes = 5;  // (1,1) (2,1) (4,1) (8,1) (16,1)
+bool g_conv_gemv_attr[64][kGvShapes];
 
-// Cluster size of the GEMV kernel: the largest of 4, 2, 1 whose slices fit the
-// shared-memory budget and whose K slice is still at least 256 long (each CTA
-// reads its slice of every position of x, so a cluster cuts the bytes each SM
-// waits for); 0 if none fits.
+// Cluster size of the GEMV kernel: the largest of 8, 4, 2, 1 whose slices fit
+// the shared-memory budget and whose K slice is still at least 64 long (each
+// CTA reads its slice of every position of x after the wait, so a larger
+// cluster cuts the bytes each SM waits for); 0 if none fits.
 int gemv_cluster(int d, int G) {
   auto fits = [&](int C) {
-    return d % (16 * C) == 0 && G >= C && gemv_smem_bytes(d, C) <= kGvSmemMax;
+    return d % (16 * C) == 0 && G >= C && gemv_smem_bytes(d, C, 1) <= kGvSmemMax;
   };
 #ifdef DFL2_GEMV_C
   if (fits(DFL2_GEMV_C)) return DFL2_GEMV_C;
 #endif
-  for (int C = 4; C >= 1; C >>= 1)
-    if (fits(C) && (C == 1 || d / C >= 256)) return C;
+  for (int C = 8; C >= 1; C >>= 1)
+    if (fits(C) && (C == 1 || d / C >= 64)) return C;
   return 0;
 }
 
 template <int C>
 cudaError_t launch_gemv_c(const ConvGemvArgs& a, cudaStream_t s, int dev) {
-  auto k = conv_gemv_kernel<C>;
-  constexpr int ci = C == 1 ? 0 : (C == 2 ? 1 : 2);
+  auto k = conv_gemv_kernel<C, 1>;
+  constexpr int ci = C == 1 ? 0 : (C == 2 ? 1 : (C == 4 ? 2 : (C == 8 ? 3 : 4)));
   if (!g_conv_gemv_attr[dev & 63][ci]) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kGvSmemMax));
     if (e != cudaSuccess) return e;
+    if (C > 8) {  // clusters of 16 are outside the portable size
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     g_conv_gemv_attr[dev & 63][ci] = true;
   }
   const int grid = (a.G + C - 1) / C * C;
-  return launch_kc(k, dim3(grid), dim3(kGvThreads), gemv_smem_bytes(a.d, C), s, true, C, a);
+  return launch_kc(k, dim3(grid), dim3(kGvThreads), gemv_smem_bytes(a.d, C, 1), s, true, C, a);
 }
-
 
 }  // namespace
 
@@ -1215,8 +1238,13 @@ cudaError_t launch_conv2(const __nv_bfloat16* x, const __nv_bfloat16* x_prev, co
   if (gv_c > 0) {
     // ---- at most 16 positions: the GEMV kernel, one group per CTA ----
     const ConvGemvArgs g{x, x_prev, base, W_c, y, R, L, d, d / kGroup, device_error_word()};
-    return gv_c == 4 ? launch_gemv_c<4>(g, s, dev)
-                     : (gv_c == 2 ? launch_gemv_c<2>(g, s, dev) : launch_gemv_c<1>(g, s, dev));
+    switch (gv_c) {
+      case 16: return launch_gemv_c<16>(g, s, dev);
+      case 8: return launch_gemv_c<8>(g, s, dev);
+      case 4: return launch_gemv_c<4>(g, s, dev);
+      case 2: return launch_gemv_c<2>(g, s, dev);
+      default: return launch_gemv_c<1>(g, s, dev);
+    }
   }
   if (R <= kSMaxRows && d % kCBK == 0 && d / kGroup >= kSGroups / 2) {
     // ---- few positions: the transposed kernel ----

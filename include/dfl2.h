@@ -195,6 +195,12 @@ dfl2_status dfl2_walk(const float* scores, const int32_t* cand_idx, int B, int L
  * at this insertion point); base float32 [2,d]; W_c bf16 [2G, d] with rows
  * [tap-0 groups; tap-1 groups].  float32 arithmetic, y rounded once to bf16
  * (nearest even).  y must not overlap x or x_prev.  No workspace.
+ * base and W_c are weights: the call may read them before it waits for the
+ * work queued ahead of it on `stream` (so that loading them overlaps that
+ * work), hence no kernel still pending on `stream` may write them (set them,
+ * e.g. with a copy, and let that copy complete or order it on another stream
+ * that the caller synchronises, before the call).  x and x_prev are read only
+ * after the earlier work on `stream` has finished.
  */
 dfl2_status dfl2_conv2(const uint16_t* x, const uint16_t* x_prev, const float* base,
                        const uint16_t* W_c, int B, int L, int d, uint16_t* y,
