@@ -298,6 +298,235 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
+// ============================================================================
+// Batched projections: each E row gathered once, N = 512.
+// ============================================================================
+// Per sequence the rows are the verified token, then the 16 L candidates
+// (position-major).  A(.) is needed for the verified token and the candidates
+// of positions 0..L-2 (the predecessors), B(.) for every candidate; the rows
+// overlap, so one GEMM [rows x d] x [d x 512] with [W_A; W_B] as N gathers each
+// E row once.  The epilogue writes columns 0..255 to PA for predecessor rows
+// and columns 256..511 to PB for candidate rows (the A of the last position's
+// candidates and the B of the verified token are computed and dropped: 1/16
+// and 1/(16L+1) of the work).  The gate rows (hidden states x W_H, N = 256)
+// are further row tiles of the same launch.
+//
+// A tile is 128 rows by 512 columns: two M=128 N=256 tcgen05 MMAs per K step,
+// the 512 float32 columns filling TMEM.  The gathered rows (16 KB per K block,
+// cp.async from random E rows) and the W tiles (64 KB per K block by TMA, L2
+// hits) travel in separate rings: 4 stages of gathered rows, kAbLag + 1 of
+// them requested ahead of the MMAs, and four 32 KB W slots (W_A's or W_B's 256
+// rows of one K block), each released as soon as its MMAs complete.  The loop
+// runs at about 0.7 us per K block at batch 64 (the MMAs alone take 0.57): the
+// gather, 128 random 128-byte pieces of E per K block and CTA, is served at
+// about 3 TB/s.  Measured no faster: N=128 MMAs on 16 KB W quarters (at N=128
+// the MMAs read shared memory twice as often per flop), 7 gather stages with
+// 6 in flight, and an L2 prefetch of the gathered rows (whole rows at once,
+// or 1 KB chunks ahead of the gather).
+constexpr int kAbAStages = 4, kAbWSlots = 4;
+constexpr int kAbLag = kAbAStages - 2;  // cp.async groups left pending behind the newest
+constexpr int kAbWQuarter = kBStage;  // one slot: 256 W rows x 64 K (32 KB)
+constexpr size_t kAbSmem = 1024 + size_t(kAbAStages) * kAStage + size_t(kAbWSlots) * kAbWQuarter + 256;
+constexpr uint32_t kAbTmemCols = 512;
+
+struct AbArgs {
+  int M_ab;           // B (16 L + 1) rows of the combined problem
+  int tiles_ab;       // ceil(M_ab / 128); the gate's tiles follow
+  int M_h;            // B L hidden rows
+  int kblocks;
+  int L, V, d;
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* hidden;
+  const __nv_bfloat16* W_A;  // L2 prefetch only (the GEMM reads W through the tensor maps)
+  const __nv_bfloat16* W_B;
+  const __nv_bfloat16* W_H;
+  const int32_t* cand_idx;  // [B,L,16]
+  const int32_t* verified;  // [B]
+  float* PA;  // [B (16 (L-1) + 1)][256]
+  float* PB;  // [B 16 L][256]
+  float* GH;  // [B L][256]
+  uint32_t* err;
+};
+
+// Source row of the combined problem (verified token or candidate), or nullptr.
+__device__ __forceinline__ const __nv_bfloat16* ab_row(const AbArgs& a, int m) {
+  if (m >= a.M_ab) return nullptr;
+  const int per = kCand * a.L + 1;
+  const int b = m / per, q = m % per;
+  const int32_t tok = q == 0 ? a.verified[b] : a.cand_idx[size_t(b) * a.L * kCand + (q - 1)];
+  if (tok < 0 || tok >= a.V) {  // never read outside E: record it and use a zero row
+    record_error(a.err, kDevErrBadIndex);
+    return nullptr;
+  }
+  return a.E + size_t(tok) * a.d;
+}
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    proj_ab_kernel(const __grid_constant__ AbArgs a, const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmH) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sA = smem;                                         // [4][128 rows][128 B]
+  uint8_t* sW = smem + size_t(kAbAStages) * kAStage;          // [4 slots][256 W rows][128 B]
+  uint64_t* a_full = reinterpret_cast<uint64_t*>(sW + size_t(kAbWSlots) * kAbWQuarter);
+  uint64_t* a_empty = a_full + kAbAStages;
+  uint64_t* w_full = a_empty + kAbAStages;
+  uint64_t* w_empty = w_full + kAbWSlots;
+  uint64_t* accum_bar = w_empty + kAbWSlots;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum_bar + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool ab = static_cast<int>(blockIdx.x) < a.tiles_ab;  // else a gate tile
+  const int m0 = (ab ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x) - a.tiles_ab) * kBM;
+  const int M = ab ? a.M_ab : a.M_h;
+  const int nq = ab ? 2 : 1;  // W slots (N = 256 each) per K block
+  const int nkb = a.kblocks;
+
+  if (tid == 0) {
+    for (int s = 0; s < kAbAStages; ++s) {
+      mbar_init(&a_full[s], 4 * 32);  // the 128 gathering threads
+      mbar_init(&a_empty[s], 1);      // one tcgen05.commit
+    }
+    for (int s = 0; s < kAbWSlots; ++s) {
+      mbar_init(&w_full[s], 1);       // the TMA expect_tx
+      mbar_init(&w_empty[s], 1);
+    }
+    mbar_init(accum_bar, 1);
+    fence_mbar_init();
+    if (ab) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+    } else {
+      tma_prefetch_desc(&tmH);
+    }
+  }
+  if (warp == 4) tmem_alloc(tmem_slot, kAbTmemCols);
+  // The W rows into L2 while the previous kernel (the top-16) still runs: a
+  // prefetch into L2 is coherent with writes in flight.  The first tile of
+  // each problem asks for its W.
+  if (m0 == 0 && tid < 256) {
+    const size_t rb = size_t(a.d) * 2;
+    if (ab) {
+      prefetch_l2_rows(a.W_A + size_t(tid) * a.d, uint32_t(rb));
+      prefetch_l2_rows(a.W_B + size_t(tid) * a.d, uint32_t(rb));
+    } else {
+      prefetch_l2_rows(a.W_H + size_t(tid) * a.d, uint32_t(rb));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // candidates may come from the previous kernel
+
+  if (warp < 4) {
+    // ---- gather: 128 rows x 128 B per K block by 16-byte cp.async, written in
+    // the 128-byte swizzle; up to kAbLag + 1 K blocks in flight ----
+    const int j = tid & 7;  // 16-byte chunk within the 128-byte row
+    const __nv_bfloat16* src[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int m = m0 + (tid >> 3) + 16 * i;
+      src[i] = ab ? ab_row(a, m) : (m < M ? a.hidden + size_t(m) * a.d : nullptr);
+    }
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kAbAStages;
+      if (it >= kAbAStages && !mbar_wait(&a_empty[s], ((it / kAbAStages) - 1) & 1, a.err))
+        record_error(a.err, kDevErrGemm);
+      const int kelem = it * kBK;
+      uint8_t* dstA = sA + size_t(s) * kAStage;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int r = (tid >> 3) + 16 * i;
+        void* dst = dstA + r * 128 + ((j ^ (r & 7)) << 4);
+        const __nv_bfloat16* g = src[i] ? src[i] + kelem + j * 8 : a.E;
+        cp_async16(dst, g, src[i] != nullptr);
+      }
+      cp_async_commit();
+      if (it >= kAbLag) {
+        cp_async_wait<kAbLag>();
+        fence_proxy_async_smem();
+        mbar_arrive(&a_full[(it - kAbLag) % kAbAStages]);
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int it = max(0, nkb - kAbLag); it < nkb; ++it) mbar_arrive(&a_full[it % kAbAStages]);
+  } else {
+    if (warp == 4 && lane == 0) {
+      // ---- MMA issuer: per K block, one N=256 MMA per W slot ----
+      const uint32_t idesc = umma_idesc_bf16(kBM, kBN);
+      for (int it = 0; it < nkb; ++it) {
+        const int sa = it % kAbAStages;
+        if (!mbar_wait(&a_full[sa], (it / kAbAStages) & 1, a.err)) record_error(a.err, kDevErrGemm);
+        const uint64_t ad = umma_desc_sw128(sA + size_t(sa) * kAStage);
+        for (int q = 0; q < nq; ++q) {
+          const int u = it * nq + q, sw = u % kAbWSlots;
+          if (!mbar_wait(&w_full[sw], (u / kAbWSlots) & 1, a.err)) record_error(a.err, kDevErrGemm);
+          tc_fence_after();
+          const uint64_t bd = umma_desc_sw128(sW + size_t(sw) * kAbWQuarter);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            umma_bf16(tmem + uint32_t(q * kBN), ad + 2 * k, bd + 2 * k, idesc,
+                      (it > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&w_empty[sw]);
+        }
+        umma_commit(&a_empty[sa]);
+      }
+      umma_commit(accum_bar);
+    } else if (warp == 5 && lane == 0) {
+      // ---- W producer: the K block's W_A then W_B tile (or W_H's) by TMA,
+      // one slot each ----
+      for (int u = 0; u < nkb * nq; ++u) {
+        const int it = u / nq, q = u % nq, sw = u % kAbWSlots;
+        if (u >= kAbWSlots && !mbar_wait(&w_empty[sw], ((u / kAbWSlots) - 1) & 1, a.err))
+          record_error(a.err, kDevErrGemm);
+        mbar_arrive_expect_tx(&w_full[sw], uint32_t(kAbWQuarter));
+        const CUtensorMap* tm = !ab ? &tmH : (q == 0 ? &tmA : &tmB);
+        tma_load_2d(sW + size_t(sw) * kAbWQuarter, tm, it * kBK, 0, &w_full[sw]);
+      }
+    }
+    __syncwarp();
+    // ---- epilogue: TMEM -> the rows' outputs ----
+    if (!mbar_wait(accum_bar, 0, a.err)) record_error(a.err, kDevErrGemm);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const int row = m0 + quarter * 32 + lane;
+    float* dst[2] = {nullptr, nullptr};
+    if (row < M) {
+      if (ab) {
+        const int per = kCand * a.L + 1;
+        const int b = row / per, q = row % per;
+        if (q <= kCand * (a.L - 1)) dst[0] = a.PA + (size_t(b) * (kCand * (a.L - 1) + 1) + q) * kRank;
+        if (q >= 1) dst[1] = a.PB + (size_t(b) * kCand * a.L + (q - 1)) * kRank;
+      } else {
+        dst[0] = a.GH + size_t(row) * kRank;
+      }
+    }
+    for (int h = 0; h < nq; ++h) {
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        float v[32];
+        tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + uint32_t(h * kBN + c * 32), v);
+        if (dst[h]) {
+          float4* o = reinterpret_cast<float4*>(dst[h] + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            o[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  pdl_launch_dependents();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kAbTmemCols);
+  }
+}
+
 struct PairArgs {
   const float* PA;  // [MA][256] (per-cycle projections), or
   const float* PB;  // [MB][256]
@@ -752,6 +981,7 @@ cudaError_t launch_pair_walk(const PairArgs& qa, int B, int L, cudaStream_t s, b
 }
 
 bool g_gemm_attr[64];
+bool g_ab_attr[64];
 
 }  // namespace
 
@@ -870,6 +1100,38 @@ static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, 
                    splits, g, tm[0], tm[1], tm[2]);
 }
 
+// The pair scores (and the fused walk) over the projections in the workspace.
+static cudaError_t launch_pair(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
+                               const float* PA, const float* PB, const float* GH, int V,
+                               float* scores, const WalkFuse* walk, void* ws, cudaStream_t s,
+                               bool pdl) {
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PairArgs qa{};
+  qa.PA = PA;
+  qa.PB = PB;
+  qa.GH = GH;
+  qa.V = V;
+  qa.err = device_error_word();
+  qa.cand_val = cand_val;
+  qa.scores = scores;
+  qa.L = p.L;
+  if (walk) {
+    qa.walk = 1;
+    qa.T = walk->T;
+    qa.seeds = walk->seeds;
+    qa.cycle = walk->cycle;
+    qa.cand_idx = cand_idx;
+    qa.tokens = walk->tokens;
+    qa.slots = walk->slots;
+    qa.q = walk->q;
+    qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
+    qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
+    qa.qrows = reinterpret_cast<float*>(w + p.q_off);
+    if (p.L <= kPwMaxL) return launch_pair_walk(qa, p.B, p.L, s, pdl);
+  }
+  return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
+}
+
 cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const float* cand_val,
                           const int32_t* verified, const __nv_bfloat16* hidden,
                           const __nv_bfloat16* E, const __nv_bfloat16* W_A,
@@ -885,15 +1147,51 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
     if (e != cudaSuccess) return e;
     g_gemm_attr[dev & 63] = true;
   }
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* PA = reinterpret_cast<float*>(w + p.PA_off);
+  float* PB = reinterpret_cast<float*>(w + p.PB_off);
+  float* GH = reinterpret_cast<float*>(w + p.GH_off);
+  if (p.splits == 1 && p.nsplit == 1) {
+    // ---- batched: one gather per E row, [W_A; W_B] as N = 512 ----
+    if (!g_ab_attr[dev & 63]) {
+      e = cudaFuncSetAttribute(proj_ab_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kAbSmem));
+      if (e != cudaSuccess) return e;
+      g_ab_attr[dev & 63] = true;
+    }
+    alignas(64) CUtensorMap tA, tB, tH;  // boxes of 64 K x 256 W rows (one slot)
+    if (!tensor_map_bf16(W_A, kRank, p.d, kBN, &tA) || !tensor_map_bf16(W_B, kRank, p.d, kBN, &tB) ||
+        !tensor_map_bf16(W_H, kRank, p.d, kBN, &tH))
+      return cudaErrorInvalidValue;
+    AbArgs g{};
+    g.M_ab = p.B * (kCand * p.L + 1);
+    g.tiles_ab = (g.M_ab + kBM - 1) / kBM;
+    g.M_h = p.MH;
+    g.kblocks = p.kblocks;
+    g.L = p.L;
+    g.V = V;
+    g.d = p.d;
+    g.E = E;
+    g.hidden = hidden;
+    g.W_A = W_A;
+    g.W_B = W_B;
+    g.W_H = W_H;
+    g.cand_idx = cand_idx;
+    g.verified = verified;
+    g.PA = PA;
+    g.PB = PB;
+    g.GH = GH;
+    g.err = device_error_word();
+    const int grid = g.tiles_ab + (p.MH + kBM - 1) / kBM;
+    e = launch_kc(proj_ab_kernel, dim3(grid), dim3(kGemmThreads), kAbSmem, s, pdl, 1, g, tA, tB, tH);
+    if (e != cudaSuccess) return e;
+    return launch_pair(p, cand_idx, cand_val, PA, PB, GH, V, scores, walk, ws, s, pdl);
+  }
   alignas(64) CUtensorMap tA, tB, tH;
   const uint32_t bn = static_cast<uint32_t>(kBN / p.nsplit);
   if (!tensor_map_bf16(W_A, kRank, p.d, bn, &tA) || !tensor_map_bf16(W_B, kRank, p.d, bn, &tB) ||
       !tensor_map_bf16(W_H, kRank, p.d, bn, &tH))
     return cudaErrorInvalidValue;
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  float* PA = reinterpret_cast<float*>(w + p.PA_off);
-  float* PB = reinterpret_cast<float*>(w + p.PB_off);
-  float* GH = reinterpret_cast<float*>(w + p.GH_off);
   GemmArgs g{};
   const int Ms[3] = {p.MA, p.MB, p.MH};
   float* outs[3] = {PA, PB, GH};
@@ -926,30 +1224,7 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   e = launch_kc(proj_tc_kernel, dim3(before * p.nsplit * p.splits), dim3(kGemmThreads), kGemmSmem,
                 s, pdl, p.splits, g, tA, tB, tH);
   if (e != cudaSuccess) return e;
-  PairArgs qa{};
-  qa.PA = PA;
-  qa.PB = PB;
-  qa.GH = GH;
-  qa.V = V;
-  qa.err = device_error_word();
-  qa.cand_val = cand_val;
-  qa.scores = scores;
-  qa.L = p.L;
-  if (walk) {
-    qa.walk = 1;
-    qa.T = walk->T;
-    qa.seeds = walk->seeds;
-    qa.cycle = walk->cycle;
-    qa.cand_idx = cand_idx;
-    qa.tokens = walk->tokens;
-    qa.slots = walk->slots;
-    qa.q = walk->q;
-    qa.tickets = reinterpret_cast<uint32_t*>(w + p.ticket_off);
-    qa.choice = reinterpret_cast<int32_t*>(w + p.choice_off);
-    qa.qrows = reinterpret_cast<float*>(w + p.q_off);
-    if (p.L <= kPwMaxL) return launch_pair_walk(qa, p.B, p.L, s, pdl);
-  }
-  return launch_k(pair16_kernel, dim3(p.B * p.L), dim3(kPairThreads), 0, s, pdl, qa);
+  return launch_pair(p, cand_idx, cand_val, PA, PB, GH, V, scores, walk, ws, s, pdl);
 }
 
 cudaError_t launch_tables_build(const __nv_bfloat16* E, const __nv_bfloat16* W_A,

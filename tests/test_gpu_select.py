@@ -91,14 +91,17 @@ def test_batched_workloads(name, nseq):
     report(kind="scores", what=f"{name} {len(seqs)} of {w.B} sequences", worst_err_over_tol=worst)
 
 
-@pytest.mark.parametrize("B,L", [(1, 1), (3, 2), (5, 17)])
-def test_edge_shapes(B, L):
-    w = wl.WORKLOADS["tiny_l8_v32k"].with_(B=B, L=L, V=4096, d=128, e_std=1.0)
+# (40, 16) and (19, 33) have enough row tiles for the batched projection (no K
+# split, every E row gathered once for both maps), with a ragged last row tile
+@pytest.mark.parametrize("B,L,d", [(1, 1, 128), (3, 2, 128), (5, 17, 128), (40, 16, 256),
+                                   (19, 33, 128)])
+def test_edge_shapes(B, L, d):
+    w = wl.WORKLOADS["tiny_l8_v32k"].with_(B=B, L=L, V=4096, d=d, e_std=1.0)
     inp = wl.make_tail_inputs(w, "cpu")
     idx, val = candidates_from_oracle(wl.make_logits(w, "cpu"))
     S = gpu_select(idx, val, inp["verified"], inp)
     ref = oracle_select_subset(idx, val, inp["verified"], inp, list(range(B)))
-    assert_scores_close(S, ref, f"B={B} L={L}")
+    assert_scores_close(S, ref, f"B={B} L={L} d={d}")
 
 
 def test_zero_W_A_gives_plain_logits():

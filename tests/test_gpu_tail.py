@@ -125,6 +125,16 @@ def test_tail_equals_the_three_calls():
     np.testing.assert_array_equal(tok.cpu().numpy(), g["tokens"])
 
 
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_batched_projection_path(T):
+    """Enough sequences for the batched projection (each E row gathered once,
+    [W_A; W_B] as one N = 512 product); the last row tile is ragged."""
+    w = wl.WORKLOADS["tiny_l8_v32k"].with_(B=40, L=16, V=4096, d=256, e_std=1.0)
+    lg = wl.make_logits(w, "cpu")
+    inp = wl.make_tail_inputs(w, "cpu")
+    check_tail(w, lg, inp, T, inp["seeds"], 3, list(range(w.B)))
+
+
 def test_minimal_block():
     w = wl.WORKLOADS["tiny_l8_v32k"].with_(L=1, V=16, d=64, e_std=1.0)
     lg = wl.make_logits(w, "cpu")
