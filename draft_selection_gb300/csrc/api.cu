@@ -155,9 +155,6 @@ dfl2_status check_topk_args(int dtype, int B, int L, int V, int k) {
     return fail(DFL2_ERR_UNSUPPORTED, "logits dtype %d is not float32 or bf16", dtype);
   if (k != dfl2::kCand) return fail(DFL2_ERR_UNSUPPORTED, "k=%d: only 16 candidates", k);
   if (V < dfl2::kCand) return fail(DFL2_ERR_INVALID_ARG, "V=%d < 16", V);
-  const int per16 = dtype == DFL2_F32 ? 4 : 8;
-  if (V % per16 != 0)
-    return fail(DFL2_ERR_UNSUPPORTED, "V=%d: logits rows must be a multiple of 16 bytes", V);
   return DFL2_OK;
 }
 
@@ -199,8 +196,8 @@ dfl2_status check_select_args(int B, int L, int V, int d, int r) {
   DFL2_TRY(check_shape(B, L));
   if (r != dfl2::kRank) return fail(DFL2_ERR_UNSUPPORTED, "r=%d: only rank 256", r);
   if (V < dfl2::kCand) return fail(DFL2_ERR_INVALID_ARG, "V=%d < 16", V);
-  if (d < 64 || d % 64 != 0)
-    return fail(DFL2_ERR_UNSUPPORTED, "d=%d: the selector needs a multiple of 64", d);
+  if (d < 16 || d % 16 != 0)
+    return fail(DFL2_ERR_UNSUPPORTED, "d=%d: the selector needs a multiple of 16", d);
   return DFL2_OK;
 }
 

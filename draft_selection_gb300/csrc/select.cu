@@ -8,9 +8,10 @@
 //       candidates of positions 0..L-2), gathered from E, times W_A^T;
 //   PB: the candidates of positions 0..L-1, gathered from E, times W_B^T;
 //   GH: the hidden states times W_H^T (pre-sigmoid).
-// Tiles are 128 rows x 256 columns, K in blocks of 64.  W tiles arrive by TMA
-// (128-byte swizzle); the gathered rows by 16-byte cp.async written in the same
-// swizzle; the accumulator lives in TMEM (256 columns).  When there are too few
+// Tiles are 128 rows x 256 columns, K in blocks of 64 (a partial last block
+// reads zeros past d: TMA out-of-bounds fill for W, zero-fill for the rows).
+// W tiles arrive by TMA (128-byte swizzle); the gathered rows by 16-byte
+// cp.async written in the same swizzle; the accumulator lives in TMEM (256 columns).  When there are too few
 // tiles to fill the GPU (batch 1), K is split over the CTAs of a thread-block
 // cluster: each CTA stages its fp32 partial tile in shared memory and stores it
 // to the caller's workspace in whole rows (the partials stay in L2), one
@@ -135,7 +136,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // flight, so it may precede the dependency wait.
   // One CTA per K range (the problem's first row tile) asks for it.
   if (P.W && nkb > 0 && m0 == 0 && tid < bn)
-    prefetch_l2_rows(P.W + size_t(n0 + tid) * a.d + size_t(kb0) * kBK, uint32_t(nkb) * kBK * 2u);
+    prefetch_l2_rows(P.W + size_t(n0 + tid) * a.d + size_t(kb0) * kBK,
+                     uint32_t(min(nkb * kBK, a.d - kb0 * kBK)) * 2u);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -158,12 +160,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         tma_load_2d(sB + size_t(s) * kBStage, tmap, kelem, n0, &full_bar[s]);
       }
       uint8_t* dstA = sA + size_t(s) * kAStage;
+      const bool kin = kelem + j * 8 < a.d;  // chunks past d (the last K block) read as zero
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = (tid >> 3) + 16 * i;
         void* dst = dstA + r * 128 + ((j ^ (r & 7)) << 4);
-        const __nv_bfloat16* g = src[i] ? src[i] + kelem + j * 8 : a.E;
-        cp_async16(dst, g, src[i] != nullptr);
+        const bool ok = src[i] != nullptr && kin;
+        cp_async16(dst, ok ? src[i] + kelem + j * 8 : a.E, ok);
       }
       cp_async_commit();
       if (it >= 2) {
@@ -436,12 +439,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         record_error(a.err, kDevErrGemm);
       const int kelem = it * kBK;
       uint8_t* dstA = sA + size_t(s) * kAStage;
+      const bool kin = kelem + j * 8 < a.d;  // chunks past d (the last K block) read as zero
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int r = (tid >> 3) + 16 * i;
         void* dst = dstA + r * 128 + ((j ^ (r & 7)) << 4);
-        const __nv_bfloat16* g = src[i] ? src[i] + kelem + j * 8 : a.E;
-        cp_async16(dst, g, src[i] != nullptr);
+        const bool ok = src[i] != nullptr && kin;
+        cp_async16(dst, ok ? src[i] + kelem + j * 8 : a.E, ok);
       }
       cp_async_commit();
       if (it >= kAbLag) {
@@ -1005,7 +1009,7 @@ SelectPlan select_plan(int B, int L, int d) {
   p.MA = B * (kCand * (L - 1) + 1);
   p.MB = B * kCand * L;
   p.MH = B * L;
-  p.kblocks = d / kBK;
+  p.kblocks = (d + kBK - 1) / kBK;  // the last block may be partial (d % 16 == 0)
   const int tiles = (p.MA + kBM - 1) / kBM + (p.MB + kBM - 1) / kBM + (p.MH + kBM - 1) / kBM;
   // Split K (over a cluster) only when the tiles cannot fill the GPU: the
   // largest power of two <= 8 that keeps tiles*splits within one wave.
@@ -1086,7 +1090,7 @@ static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, 
   g.splits = splits;
   g.nsplit = 1;
   g.kps = kps;
-  g.kblocks = d / kBK;
+  g.kblocks = (d + kBK - 1) / kBK;
   g.E = E;
   g.hidden = hidden;
   g.cand_idx = cand_idx;
@@ -1232,7 +1236,7 @@ cudaError_t launch_tables_build(const __nv_bfloat16* E, const __nv_bfloat16* W_A
                                 cudaStream_t s) {
   // every row of E times W_A^T and W_B^T: one launch, two problems, K unsplit
   const ProjJob jobs[2] = {{kRowsE, V, P_A, W_A}, {kRowsE, V, P_B, W_B}};
-  return launch_proj_jobs(jobs, 2, 1, d / kBK, d, E, nullptr, nullptr, nullptr, 1, V, nullptr, s,
+  return launch_proj_jobs(jobs, 2, 1, (d + kBK - 1) / kBK, d, E, nullptr, nullptr, nullptr, 1, V, nullptr, s,
                           true);
 }
 

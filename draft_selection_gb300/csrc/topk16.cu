@@ -59,7 +59,7 @@ static_assert(kStages >= kConsumerWarps, "the held bound tiles must fit in the r
 
 struct TopkArgs {
   const uint8_t* logits;
-  int V;
+  int V, rows;
   int tiles_per_row;
   long long total_tiles;
   int max_contrib;
@@ -318,6 +318,87 @@ __device__ __forceinline__ float lane_max_tile(const uint4* tile, int nvec, int 
   return m;
 }
 
+
+// A logits row as streamed: the 16-byte-aligned window [lo, hi) of the flat
+// logits buffer around the row's bytes [s, e).  Rows need not start on 16
+// bytes (V * element size may be any even number); the buffer's bytes past its
+// last whole 16 bytes (floor16) cannot be bulk-copied and are read by plain
+// loads (finish_tile).
+struct RowWin {
+  size_t s, e, lo, hi;
+};
+__device__ __forceinline__ RowWin row_window(long long row, size_t rb, size_t floor16) {
+  RowWin w;
+  w.s = size_t(row) * rb;
+  w.e = w.s + rb;
+  w.lo = w.s & ~size_t(15);
+  w.hi = min((w.e + 15) & ~size_t(15), floor16);
+  return w;
+}
+// Bytes the bulk copy moves for tile t of a window (0 past its end).
+__device__ __forceinline__ uint32_t tile_bytes(const RowWin& w, int t) {
+  const size_t a = w.lo + size_t(t) * kTileBytes;
+  return a < w.hi ? static_cast<uint32_t>(min(size_t(kTileBytes), w.hi - a)) : 0u;
+}
+// Row index of tile t's first element, as a 32-bit value that wraps below 0
+// (the window may start up to 7 elements before the row).
+template <int EPV>
+__device__ __forceinline__ uint32_t tile_ebase(const RowWin& w, int t) {
+  constexpr int es = 16 / EPV;
+  return static_cast<uint32_t>(static_cast<long long>(t) * (kTileBytes / es) -
+                               static_cast<long long>((w.s - w.lo) / es));
+}
+// Completes a staged tile before the one warp that scans it does so.  The
+// window's elements outside the row (before its start, after its end) become
+// -inf: their keys carry indices outside [0, V), which rank below every
+// element of the row, so with V >= 16 none is ever selected.  The row's
+// elements past the buffer's last whole 16 bytes (its last row only) are read
+// with plain loads into the vector after the copied bytes.  Every lane calls
+// it; returns the tile's vector count.
+template <int EPV>
+__device__ __forceinline__ int finish_tile(uint8_t* tile, int t, const RowWin& w, size_t floor16,
+                                           const uint8_t* logits, int lane) {
+  constexpr int es = 16 / EPV;
+  const size_t a = w.lo + size_t(t) * kTileBytes;  // flat byte of the tile's start
+  int nbytes = static_cast<int>(tile_bytes(w, t));
+  if (lane == 0 && ((w.s | w.e) & 15)) {
+    auto neg_inf = [&](size_t g) {  // element at flat byte g of this tile
+      if constexpr (es == 2)
+        *reinterpret_cast<uint16_t*>(tile + (g - a)) = 0xFF80u;
+      else
+        *reinterpret_cast<uint32_t*>(tile + (g - a)) = 0xFF800000u;
+    };
+    bool wrote = false;
+    if (w.e > floor16 && floor16 >= a && floor16 < a + kTileBytes) {
+      for (size_t g = floor16; g < floor16 + 16; g += es) {
+        if (g < w.e) {
+          if constexpr (es == 2)
+            *reinterpret_cast<uint16_t*>(tile + (g - a)) = *reinterpret_cast<const uint16_t*>(logits + g);
+          else
+            *reinterpret_cast<uint32_t*>(tile + (g - a)) = *reinterpret_cast<const uint32_t*>(logits + g);
+        } else {
+          neg_inf(g);
+        }
+      }
+      nbytes = static_cast<int>(floor16 - a) + 16;
+      wrote = true;
+    }
+    if (t == 0 && w.s > w.lo) {
+      for (size_t g = w.lo; g < w.s; g += es) neg_inf(g);
+      wrote = true;
+    }
+    if ((w.e & 15) && w.e <= floor16 && w.e >= a && w.e < a + size_t(nbytes)) {
+      for (size_t g = w.e; g < ((w.e + 15) & ~size_t(15)); g += es) neg_inf(g);
+      wrote = true;
+    }
+    // these generic writes come before the next bulk copy into the stage
+    if (wrote) fence_proxy_async_smem();
+  }
+  nbytes = __shfl_sync(kFull, nbytes, 0);
+  __syncwarp();
+  return nbytes / 16;
+}
+
 __device__ __forceinline__ void write_row(const TopkArgs& a, long long row, uint64_t key, int lane) {
   if (lane < kCand) {
     a.out_idx[row * kCand + lane] = static_cast<int32_t>(~static_cast<uint32_t>(key));
@@ -390,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
   const long long g0 = (long long)c * T / G, g1 = (long long)(c + 1) * T / G;
   const int tpr = a.tiles_per_row;
   const size_t row_bytes = size_t(a.V) * (16 / EPV);
+  const size_t floor16 = (size_t(a.rows) * row_bytes) & ~size_t(15);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -412,11 +494,12 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
       const int n = static_cast<int>(g1 - g0);
       for (int i = 0, s = 0, ph = 0; i < n; ++i) {
         if (i >= kStages && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
-        const size_t off = size_t(t) * kTileBytes;
-        const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
+        const RowWin win = row_window(row, row_bytes, floor16);
+        const uint32_t bytes = tile_bytes(win, t);
         mbar_arrive_expect_tx(&full_bar[s], bytes);
-        bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + size_t(row) * row_bytes + off, bytes,
-                 &full_bar[s]);
+        if (bytes)
+          bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + win.lo + size_t(t) * kTileBytes,
+                   bytes, &full_bar[s]);
         st_release_cta(issued, static_cast<uint32_t>(i + 1));
         if (++t == tpr) {
           t = 0;
@@ -455,8 +538,9 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
           !mbar_wait(&full_bar[st], (i / kStages) & 1, a.err))
         record_error(a.err, kDevErrTopkFull);
       const int t = t0 + j;
-      nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
-      elem_base = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
+      const RowWin win = row_window(row, row_bytes, floor16);
+      nvec = finish_tile<EPV>(stages + size_t(st) * kTileBytes, t, win, floor16, a.logits, lane);
+      elem_base = tile_ebase<EPV>(win, t);
       tile = reinterpret_cast<const uint4*>(stages + size_t(st) * kTileBytes);
     };
     auto release = [&](int j) {
@@ -622,7 +706,7 @@ static_assert(kConsumerWarps <= kRMaxCluster, "lists ranked by rank_sorted_lists
 
 struct RowsArgs {
   const uint8_t* logits;
-  int V, tiles_per_row, C;
+  int V, rows, tiles_per_row, C;
   int32_t* out_idx;
   float* out_val;
   uint32_t* err;
@@ -775,6 +859,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   const int t_lo = rank * tpr / C, t_hi = (rank + 1) * tpr / C;  // this CTA's tiles of the row
   const int n = t_hi - t_lo;
   const size_t row_bytes = size_t(a.V) * (16 / EPV);
+  const size_t floor16 = (size_t(a.rows) * row_bytes) & ~size_t(15);
+  const RowWin win = row_window(row, row_bytes, floor16);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kRStages; ++s) {
@@ -799,11 +885,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
     if (lane == 0) {
       for (int i = 0, s = 0, ph = 0; i < n; ++i) {
         if (i >= kRStages && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
-        const size_t off = size_t(t_lo + i) * kTileBytes;
-        const uint32_t bytes = static_cast<uint32_t>(min(size_t(kTileBytes), row_bytes - off));
+        const uint32_t bytes = tile_bytes(win, t_lo + i);
         mbar_arrive_expect_tx(&full_bar[s], bytes);
-        bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + size_t(row) * row_bytes + off, bytes,
-                 &full_bar[s]);
+        if (bytes)
+          bulk_g2s(stages + size_t(s) * kTileBytes,
+                   a.logits + win.lo + size_t(t_lo + i) * kTileBytes, bytes, &full_bar[s]);
         st_release_cta(issued, static_cast<uint32_t>(i + 1));
         if (++s == kRStages) {
           s = 0;
@@ -820,8 +906,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
           !mbar_wait(&full_bar[st], (i / kRStages) & 1, a.err))
         record_error(a.err, kDevErrTopkFull);
       const int t = t_lo + i;
-      nvec = static_cast<int>(min(size_t(kTileBytes), row_bytes - size_t(t) * kTileBytes) / 16);
-      eb = static_cast<uint32_t>(t) * (kTileBytes / (16 / EPV));
+      nvec = finish_tile<EPV>(stages + size_t(st) * kTileBytes, t, win, floor16, a.logits, lane);
+      eb = tile_ebase<EPV>(win, t);
       tile = reinterpret_cast<const uint4*>(stages + size_t(st) * kTileBytes);
     };
     WarpTop w{0ull, -INFINITY};
@@ -964,11 +1050,14 @@ TopkPlan topk_plan(int rows, int V, int elem_bytes) {
   p.rows = rows;
   p.V = V;
   p.elem_bytes = elem_bytes;
-  p.tiles_per_row = static_cast<int>((size_t(V) * elem_bytes + kTileBytes - 1) / kTileBytes);
+  // tiles of a row's 16-byte-aligned window (up to 30 bytes wider than the row
+  // when rows do not start on 16 bytes)
+  const size_t rb = size_t(V) * elem_bytes, win = rb % 16 ? rb + 30 : rb;
+  p.tiles_per_row = static_cast<int>((win + kTileBytes - 1) / kTileBytes);
   // Workspace stride: contributors per row are at most the row's tiles and at
   // most ceil(grid / rows) + 1; sized for float32 rows and the largest grid so
   // the size does not depend on the device or the dtype.
-  const long long tiles_f32 = (size_t(V) * 4 + kTileBytes - 1) / kTileBytes;
+  const long long tiles_f32 = (size_t(V) * 4 + 30 + kTileBytes - 1) / kTileBytes;
   p.max_contrib = static_cast<int>(std::min<long long>(tiles_f32, (kMaxGrid + rows - 1) / rows + 1));
   p.partial_off = 256;
   p.ticket_off = align_up(p.partial_off + size_t(rows) * p.max_contrib * kCand * 8, 256);
@@ -996,6 +1085,7 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
       RowsArgs r;
       r.logits = static_cast<const uint8_t*>(logits);
       r.V = plan.V;
+      r.rows = plan.rows;
       r.tiles_per_row = plan.tiles_per_row;
       r.C = C;
       r.out_idx = idx;
@@ -1017,6 +1107,7 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
   TopkArgs a;
   a.logits = static_cast<const uint8_t*>(logits);
   a.V = plan.V;
+  a.rows = plan.rows;
   a.tiles_per_row = plan.tiles_per_row;
   a.total_tiles = T;
   a.max_contrib = plan.max_contrib;

@@ -39,9 +39,9 @@
  *     DFL2_ERR_CUDA.  No call throws, aborts or prints.  dfl2_last_error()
  *     returns a thread-local message for the last failing call.
  *   - Fixed method sizes: k = 16 candidates, r = 256 selector rank; d must be a
- *     multiple of 64 for dfl2_select and of 16 for dfl2_conv2; V >= 16, L >= 1,
- *     B >= 1.  Logits rows must be a whole number of 16-byte units (V % 8 == 0
- *     for bf16, V % 4 == 0 for float32).
+ *     multiple of 16; V >= 16 (any V: logits rows need not start on 16 bytes),
+ *     L >= 1, B >= 1.  The entry points of the NEXT rows keep narrower limits,
+ *     stated at each (dfl2_verify: V % 4 == 0; dfl2_lmhead_topk: d % 8 == 0).
  *   - Every wait inside a kernel is bounded.  A wait that runs out (about 2 s
  *     of SM clock) records a code in a per-device error word
  *     (dfl2_device_error) and the kernel carries on without the data it

@@ -53,8 +53,9 @@ def test_topk_rejects_bad_arguments(lib):
     f = lib.dfl2_topk
     assert f(A, 1, 1, 8, 1024, 17, A, A, A, ws, None) == UNSUPPORTED      # k != 16
     assert f(A, 7, 1, 8, 1024, 16, A, A, A, ws, None) == UNSUPPORTED      # dtype
-    assert f(A, 1, 1, 8, 1020, 16, A, A, A, ws, None) == UNSUPPORTED      # bf16 rows not 16 B
-    assert f(A, 0, 1, 8, 1022, 16, A, A, A, ws, None) == UNSUPPORTED      # f32 rows not 16 B
+    # rows that do not start on 16 bytes are accepted (the checks go on to the workspace)
+    assert f(A, 1, 1, 8, 50257, 16, A, A, A, 0, None) == WORKSPACE       # bf16, V odd
+    assert f(A, 0, 1, 8, 1022, 16, A, A, A, 0, None) == WORKSPACE        # f32, V % 4 != 0
     assert f(A, 1, 1, 8, 8, 16, A, A, A, ws, None) == INVALID             # V < 16
     assert f(A, 1, 0, 8, 1024, 16, A, A, A, ws, None) == INVALID          # B = 0
     assert f(A, 1, 1, 0, 1024, 16, A, A, A, ws, None) == INVALID          # L = 0
@@ -85,7 +86,8 @@ def test_select_rejects_bad_arguments(lib):
     f = lib.dfl2_select
     good = [A] * 8
     assert f(*good, 1, 8, 32768, 1024, 255, A, A, ws, None) == UNSUPPORTED   # r != 256
-    assert f(*good, 1, 8, 32768, 1000, 256, A, A, ws, None) == UNSUPPORTED   # d % 64
+    assert f(*good, 1, 8, 32768, 1000, 256, A, A, ws, None) == UNSUPPORTED   # d % 16
+    assert f(*good, 1, 8, 32768, 2576, 256, A, A, 16, None) == WORKSPACE     # d % 16 == 0 accepted
     assert f(*good, 1, 8, 8, 1024, 256, A, A, ws, None) == INVALID           # V < 16
     bad = list(good)
     bad[4] = None                                                             # NULL E
@@ -126,7 +128,7 @@ def test_tables_reject_bad_arguments(lib):
     assert dfl2.dfl2_tables_bytes(151936) == 151936 * 256 * 4
     assert dfl2.dfl2_tables_bytes(8) == 0
     f = lib.dfl2_tables_build
-    assert f(A, A, A, 1024, 100, A2, A2 + 0x100000, None) == UNSUPPORTED      # d % 64
+    assert f(A, A, A, 1024, 100, A2, A2 + 0x100000, None) == UNSUPPORTED      # d % 16
     assert f(A, A, A, 8, 1024, A2, A2 + 0x100000, None) == INVALID             # V < 16
     assert f(A, None, A, 1024, 1024, A2, A2 + 0x100000, None) == INVALID       # NULL W_A
     g = lib.dfl2_select_tables
@@ -182,7 +184,10 @@ def test_tail_rejects_bad_arguments(lib):
     st = f(*args(seeds=None, T=0.0))   # greedy needs no seeds: whatever fails next, not that
     assert st != OK and "seeds" not in dfl2.dfl2_last_error()
     assert f(*args(d=2500)) == UNSUPPORTED
-    assert f(*args(V=151930)) == UNSUPPORTED
+    # any V >= 16 and any d % 16 == 0 pass the shape checks (they fail on the workspace)
+    ws2 = dfl2.dfl2_tail_workspace_size(1, 16, 50257, 2576)
+    assert ws2 > 0
+    assert f(*args(V=50257, d=2576, ws=ws2 - 256)) == WORKSPACE
     assert f(*args(ws=ws - 256)) == WORKSPACE
 
 

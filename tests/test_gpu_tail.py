@@ -135,6 +135,23 @@ def test_batched_projection_path(T):
     check_tail(w, lg, inp, T, inp["seeds"], 3, list(range(w.B)))
 
 
+@pytest.mark.parametrize("B,L,V,d,T", [
+    (1, 5, 50257, 2576, 1.0),   # batch 1: split K over a cluster, a 16-wide last K block
+    (3, 16, 50257, 2576, 0.0),  # a few sequences, odd vocabulary
+    (40, 16, 4099, 2576, 1.0),  # the batched projection ([W_A; W_B] as N = 512)
+    (2, 8, 1021, 1040, 0.0),    # float32 logits of an odd length, d = 1040
+])
+def test_any_vocabulary_and_hidden_size(B, L, V, d, T):
+    """Every V >= 16 and every d that is a multiple of 16: logits rows that do not
+    start on 16 bytes, and a last K block of the projections that is only partly
+    inside d."""
+    base = "tiny_l8_v32k" if d == 1040 else "drafter4b_l16"
+    w = wl.WORKLOADS[base].with_(B=B, L=L, V=V, d=d, e_std=1.0)
+    lg = wl.make_logits(w, "cpu")
+    inp = wl.make_tail_inputs(w, "cpu")
+    check_tail(w, lg, inp, T, inp["seeds"], 9, list(range(B)))
+
+
 def test_minimal_block():
     w = wl.WORKLOADS["tiny_l8_v32k"].with_(L=1, V=16, d=64, e_std=1.0)
     lg = wl.make_logits(w, "cpu")

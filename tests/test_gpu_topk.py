@@ -138,6 +138,35 @@ def test_edge_shapes(B, L, V, dt):
     check_rows(lg, idx, val)
 
 
+@pytest.mark.parametrize("B,L,V,dt", [
+    (1, 7, 50257, torch.bfloat16),   # rows start anywhere in a 16-byte unit: cluster kernel
+    (64, 16, 50257, torch.bfloat16),  # the same, rows split across CTAs: persistent kernel
+    (3, 5, 1021, torch.float32),     # float32 rows of an odd length
+    (40, 16, 1023, torch.float32),   # many short odd rows (several per CTA)
+    (1, 3, 17, torch.bfloat16),      # one past the minimum: rows of 34 bytes
+    (5, 3, 4099, torch.bfloat16),    # the buffer ends 10 bytes past its last whole 16
+    (37, 9, 1023, torch.float32),    # the same in the persistent kernel (float32)
+    (63, 5, 50257, torch.bfloat16),  # and bf16
+])
+def test_unaligned_rows(B, L, V, dt):
+    """Rows whose start is not a multiple of 16 bytes: each is streamed as the
+    aligned window around it, the neighbours' elements masked, and the bytes past
+    the buffer's last whole 16 read with plain loads."""
+    g = torch.Generator().manual_seed(B * 7 + L * 3 + V)
+    lg = (torch.randn(B, L, V, generator=g) * 3).to(dt)
+    idx, val = gpu_topk(lg.cuda())
+    check_rows(lg, idx, val)
+    # winners at the very first and last elements of every row, -inf everywhere else
+    x = torch.full((B, L, V), float("-inf"))
+    x[..., 0] = 2.0
+    x[..., -1] = 3.0
+    x = x.to(dt)
+    idx, val = gpu_topk(x.cuda())
+    check_rows(x, idx, val)
+    assert (idx[..., 0] == V - 1).all() and (idx[..., 1] == 0).all()
+    assert (idx >= 0).all() and (idx < V).all()
+
+
 def test_degenerate_rows():
     V = 4096
     rows = []
