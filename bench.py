@@ -39,9 +39,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # kernel, by (op, workload), from one ncu capture of the kernel as it is now;
 # an op whose kernel changed since its capture has no entry and reports null.
 NCU_TRAFFIC = {
-    ("topk", "drafter4b_l16"): 4939520,
-    ("topk", "serving_b64"): 314433792,
-    ("conv", "drafter4b_l16"): 1759744,
+    ("topk", "drafter4b_l16"): 4940544,
+    ("topk", "serving_b64"): 314409728,
+    ("conv", "drafter4b_l16"): 1761024,
     ("conv", "serving_b64"): 7291136,
     ("lmhead", "drafter4b_l16"): 781673728,
     ("lmhead", "serving_b64"): 786832384,
