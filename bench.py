@@ -383,6 +383,21 @@ def measure_native(case: Case, steps: int, warmup: int, flush, pk, which):
                      "tail_bytes": ttb,
                      "tail_frac_of_hbm": round(ttb / (tt * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
     del case.PA, case.PB
+    if w.B == 1:
+        # the split-K projection on its warp-level engine (mma.sync), same graphs
+        prev = case.dfl2.dfl2_set_projection_engine(case.dfl2.PROJ_WARP)
+        try:
+            g_tw, _ = capture(case.tail)
+            case.topk()
+            g_sw, _ = capture(case.select)
+        finally:
+            case.dfl2.dfl2_set_projection_engine(prev)
+        res["proj_engines"] = {
+            "tensor": {"tail_us": round(res["tail"]["mean_ms"] * 1e3, 2),
+                       "select_us": round(res["select"]["mean_ms"] * 1e3, 2)},
+            "warp": {"tail_us": round(summarize(time_graph(g_tw, sub, warmup, flush))["mean_ms"] * 1e3, 2),
+                     "select_us": round(summarize(time_graph(g_sw, sub, warmup, flush))["mean_ms"] * 1e3, 2)},
+        }
     peak = pk["hbm_gbs"]
     shares = {"topk": res["topk"]["mean_ms"], "select": res["select"]["mean_ms"],
               "walk": res["walk"]["mean_ms"], "conv": res["conv"]["mean_ms"] * w.conv_calls}
@@ -615,6 +630,8 @@ def profile_op(args) -> int:
     import draft_selection_gb300 as dfl2
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
+    if args.proj_engine == "warp":
+        dfl2.dfl2_set_projection_engine(dfl2.PROJ_WARP)
     if args.profile_op == "lmhead":
         w = wl.WORKLOADS[args.workload]
         lm = wl.make_lmhead_inputs(w, dev, "gauss")
@@ -655,6 +672,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--sustain-s", type=float, default=3.0,
                     help="seconds of back-to-back steps after the timed region")
+    ap.add_argument("--proj-engine", choices=["tensor", "warp"], default="tensor",
+                    help="engine of the split-K projection in --profile-op runs")
     ap.add_argument("--profile-op",
                     choices=["topk", "select", "walk", "conv", "conv_plain", "tail", "step",
                              "lmhead"],
@@ -754,6 +773,7 @@ def main():
             "roofline": res["per_kernel"][res["dominant"]] | {"kernel": res["dominant"]},
             "per_kernel": res["per_kernel"],
             "tables": res["tables"],
+            "proj_engines": res.get("proj_engines"),
             "b64": batched,
             "verify": verify,
             "lmhead_topk": lmhead,

@@ -50,6 +50,8 @@ def load():
     L.dfl2_last_error.restype = SZ
     L.dfl2_launch_count.restype = U64
     L.dfl2_workspace_init.argtypes = [P, SZ, P]
+    L.dfl2_set_projection_engine.argtypes = [I]
+    L.dfl2_set_projection_engine.restype = I
     L.dfl2_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), I]
     L.dfl2_topk_workspace_size.argtypes = [I, I, I]
     L.dfl2_topk_workspace_size.restype = SZ
@@ -132,6 +134,17 @@ def dfl2_version() -> str:
 
 def dfl2_launch_count() -> int:
     return int(load().dfl2_launch_count())
+
+
+PROJ_TENSOR, PROJ_WARP = 0, 1
+
+
+def dfl2_set_projection_engine(engine: int) -> int:
+    """Engine of the split-K projection GEMM (PROJ_TENSOR or PROJ_WARP); returns the previous one."""
+    prev = int(load().dfl2_set_projection_engine(int(engine)))
+    if prev < 0:
+        raise ValueError(f"unknown projection engine {engine}")
+    return prev
 
 
 def dfl2_workspace_init(ws, nbytes: int | None = None, stream=None) -> None:

@@ -240,6 +240,11 @@ size_t dfl2_last_error(char* buf, size_t len) {
 
 uint64_t dfl2_launch_count(void) { return g_launches.load(); }
 
+int dfl2_set_projection_engine(int engine) {
+  if (engine != DFL2_PROJ_TENSOR && engine != DFL2_PROJ_WARP) return -1;
+  return dfl2::set_projection_engine(engine);
+}
+
 dfl2_status dfl2_workspace_init(void* ws, size_t ws_bytes, dfl2_stream stream) {
   DFL2_TRY(ensure_device());
   if (!ws || ws_bytes == 0) return fail(DFL2_ERR_INVALID_ARG, "empty workspace");

@@ -162,6 +162,25 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ---- warp-level tensor-core MMA (mma.sync) --------------------------------
+// ldmatrix: lane i gives the shared-memory address of row i % 8 of matrix i / 8.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t r[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t r[2]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r[0]), "=r"(r[1])
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816_bf16(float d[4], const uint32_t a[4], const uint32_t b[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
 // ---- programmatic dependent launch ----------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
@@ -235,6 +254,8 @@ struct SelectPlan {
   size_t ws_bytes;
 };
 SelectPlan select_plan(int B, int L, int d);
+// Engine of the split-K projection (DFL2_PROJ_TENSOR / DFL2_PROJ_WARP); returns the previous one.
+int set_projection_engine(int engine);
 // Precomputed token tables P_A = E W_A^T, P_B = E W_B^T (float32 [V][256]).
 cudaError_t launch_tables_build(const __nv_bfloat16* E, const __nv_bfloat16* W_A,
                                 const __nv_bfloat16* W_B, int V, int d, float* P_A, float* P_B,

@@ -31,9 +31,11 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
+#include "dfl2.h"
 #include "dfl2_internal.cuh"
 
 namespace dfl2 {
@@ -95,6 +97,12 @@ __device__ __forceinline__ const __nv_bfloat16* a_row(const GemmArgs& a, int kin
   return a.E + size_t(tok) * a.d;
 }
 
+// WARP = false: tcgen05 MMAs issued by one thread into a TMEM accumulator.
+// WARP = true (CTAs of 128 output columns only): the warp-level engine, each
+// of warps 4-7 owning 32 output columns of all 128 rows (its slice of W is read
+// by that warp alone), m16n8k16 mma.sync from the same staged tiles through
+// ldmatrix, fp32 accumulators in registers.
+template <bool WARP>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     proj_tc_kernel(const __grid_constant__ GemmArgs a, const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmH) {
@@ -124,13 +132,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kGStages; ++s) {
       mbar_init(&full_bar[s], 4 * 32 + 1);  // 128 cp.async arrivals + the TMA expect_tx
-      mbar_init(&empty_bar[s], 1);          // one tcgen05.commit
+      mbar_init(&empty_bar[s], WARP ? 4 : 1);  // one tcgen05.commit, or each MMA warp
     }
     mbar_init(accum_bar, 1);
     fence_mbar_init();
     tma_prefetch_desc(tmap);
   }
-  if (warp == 4) tmem_alloc(tmem_slot, kTmemCols);
+  if (!WARP && warp == 4) tmem_alloc(tmem_slot, kTmemCols);
   // This CTA's K range of the 256 W rows into L2 while the previous kernel
   // (the top-16) still runs: a prefetch into L2 is coherent with writes in
   // flight, so it may precede the dependency wait.
@@ -141,7 +149,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
+  const uint32_t tmem = WARP ? 0u : *tmem_slot;
   pdl_wait();  // candidates may come from the previous kernel
 
   if (warp < 4) {
@@ -178,6 +186,66 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     cp_async_wait<0>();
     fence_proxy_async_smem();
     for (int it = max(0, nkb - 2); it < nkb; ++it) mbar_arrive(&full_bar[it % kGStages]);
+  } else if constexpr (WARP) {
+    // ---- warp-level MMA: this warp's 32 output columns of all 128 rows ----
+    const int cw = (warp - 4) * 32;
+    const int mi = lane >> 3, rr = lane & 7;
+    float acc[kBM / 16][4][4];
+#pragma unroll
+    for (int mt = 0; mt < kBM / 16; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kGStages;
+      if (!mbar_wait(&full_bar[s], (it / kGStages) & 1, a.err)) record_error(a.err, kDevErrGemm);
+      const uint32_t sa = smem_u32(sA + size_t(s) * kAStage);
+      const uint32_t sb = smem_u32(sB + size_t(s) * kBStage);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        // B fragments of the four n8 tiles: W rows (output columns) x 16 K, two
+        // tiles per ldmatrix.x4 (matrices: n 0-7 K lo, n 0-7 K hi, n 8-15 K lo, K hi)
+        uint32_t bfr[4][2];
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int n = cw + np * 16 + (mi >> 1) * 8 + rr;
+          const int ch = 2 * kk + (mi & 1);  // 16-byte chunk of the 128-byte row, swizzled
+          uint32_t r[4];
+          ldsm_x4(sb + uint32_t(n) * 128u + uint32_t((ch ^ (n & 7)) << 4), r);
+          bfr[2 * np][0] = r[0];
+          bfr[2 * np][1] = r[1];
+          bfr[2 * np + 1][0] = r[2];
+          bfr[2 * np + 1][1] = r[3];
+        }
+#pragma unroll
+        for (int mt = 0; mt < kBM / 16; ++mt) {
+          // A fragment: rows mt*16.. x 16 K (matrices: rows 0-7 K lo, 8-15 K lo, 0-7 K hi, 8-15 K hi)
+          const int row = mt * 16 + (mi & 1) * 8 + rr;
+          const int ch = 2 * kk + (mi >> 1);
+          uint32_t af[4];
+          ldsm_x4(sa + uint32_t(row) * 128u + uint32_t((ch ^ (row & 7)) << 4), af);
+#pragma unroll
+          for (int nt = 0; nt < 4; ++nt) mma_16816_bf16(acc[mt][nt], af, bfr[nt]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[s]);
+    }
+    // every MMA warp is past its last ldmatrix before the staging overwrites the stages
+    named_sync(1, 128);
+    // accumulators -> the staged tile (rows kBN + 4 floats apart): c0,c1 at
+    // (row g, columns 2t, 2t+1), c2,c3 at row g + 8
+    float* stage = reinterpret_cast<float*>(smem);
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int mt = 0; mt < kBM / 16; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int col = cw + nt * 8 + 2 * t;
+        *reinterpret_cast<float2*>(stage + size_t(mt * 16 + g) * (kBN + 4) + col) =
+            make_float2(acc[mt][nt][0], acc[mt][nt][1]);
+        *reinterpret_cast<float2*>(stage + size_t(mt * 16 + g + 8) * (kBN + 4) + col) =
+            make_float2(acc[mt][nt][2], acc[mt][nt][3]);
+      }
   } else {
     if (warp == 4 && lane == 0) {
       // ---- MMA issuer ----
@@ -216,6 +284,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   tc_fence_before();
+  if (WARP && a.splits == 1) {
+    // ---- one split: the staged tile -> the output rows ----
+    __syncthreads();
+    const int rows = max(0, min(kBM, P.M - m0));
+    const float* stage = reinterpret_cast<const float*>(smem);
+    for (int e = tid; e < rows * (bn / 4); e += kGemmThreads) {
+      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      *reinterpret_cast<float4*>(P.out + size_t(m0 + lr) * kBN + n0 + 4 * c4) =
+          *reinterpret_cast<const float4*>(stage + size_t(lr) * (kBN + 4) + 4 * c4);
+    }
+    pdl_launch_dependents();
+    return;
+  }
   if (a.splits == 1) {
     __syncthreads();
     pdl_launch_dependents();
@@ -237,7 +318,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int S = a.splits;
   float* mypart = P.part + (size_t(split) * P.M) * kBN;
   float* stage = reinterpret_cast<float*>(smem);
-  if (warp >= 4) {
+  if (!WARP && warp >= 4) {  // (the warp engine staged its tile already)
     const int quarter = warp & 3;
     const int lrow = quarter * 32 + lane;
 #pragma unroll 1
@@ -260,7 +341,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   }
   cluster_sync_all();  // every split's partial tile is in the workspace
-  if (warp == 4) {
+  if (!WARP && warp == 4) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -985,6 +1066,8 @@ cudaError_t launch_pair_walk(const PairArgs& qa, int B, int L, cudaStream_t s, b
 }
 
 bool g_gemm_attr[64];
+bool g_gemm_warp_attr[64];
+std::atomic<int> g_proj_engine{DFL2_PROJ_TENSOR};
 bool g_ab_attr[64];
 
 }  // namespace
@@ -1000,6 +1083,8 @@ static void gate_split(int MH, int kblocks, int& splits, int& kps) {
   kps = (kblocks + splits - 1) / splits;
   splits = (kblocks + kps - 1) / kps;
 }
+
+int set_projection_engine(int engine) { return g_proj_engine.exchange(engine); }
 
 SelectPlan select_plan(int B, int L, int d) {
   SelectPlan p{};
@@ -1056,7 +1141,7 @@ static cudaError_t ensure_gemm_attr() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (!g_gemm_attr[dev & 63]) {
-    e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(proj_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
     g_gemm_attr[dev & 63] = true;
@@ -1100,7 +1185,7 @@ static cudaError_t launch_proj_jobs(const ProjJob* jobs, int njobs, int splits, 
   g.d = d;
   g.err = device_error_word();
   if (before == 0) return cudaSuccess;
-  return launch_kc(proj_tc_kernel, dim3(before * splits), dim3(kGemmThreads), kGemmSmem, s, pdl,
+  return launch_kc(proj_tc_kernel<false>, dim3(before * splits), dim3(kGemmThreads), kGemmSmem, s, pdl,
                    splits, g, tm[0], tm[1], tm[2]);
 }
 
@@ -1146,7 +1231,7 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (!g_gemm_attr[dev & 63]) {
-    e = cudaFuncSetAttribute(proj_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(proj_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kGemmSmem));
     if (e != cudaSuccess) return e;
     g_gemm_attr[dev & 63] = true;
@@ -1225,8 +1310,20 @@ cudaError_t launch_select(const SelectPlan& p, const int32_t* cand_idx, const fl
   g.V = V;
   g.d = p.d;
   g.err = device_error_word();
-  e = launch_kc(proj_tc_kernel, dim3(before * p.nsplit * p.splits), dim3(kGemmThreads), kGemmSmem,
-                s, pdl, p.splits, g, tA, tB, tH);
+  // the warp-level engine when asked for and the CTAs hold 128 output columns
+  if (g_proj_engine.load(std::memory_order_relaxed) == DFL2_PROJ_WARP && bn == 128) {
+    if (!g_gemm_warp_attr[dev & 63]) {
+      e = cudaFuncSetAttribute(proj_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kGemmSmem));
+      if (e != cudaSuccess) return e;
+      g_gemm_warp_attr[dev & 63] = true;
+    }
+    e = launch_kc(proj_tc_kernel<true>, dim3(before * p.nsplit * p.splits), dim3(kGemmThreads),
+                  kGemmSmem, s, pdl, p.splits, g, tA, tB, tH);
+  } else {
+    e = launch_kc(proj_tc_kernel<false>, dim3(before * p.nsplit * p.splits), dim3(kGemmThreads),
+                  kGemmSmem, s, pdl, p.splits, g, tA, tB, tH);
+  }
   if (e != cudaSuccess) return e;
   return launch_pair(p, cand_idx, cand_val, PA, PB, GH, V, scores, walk, ws, s, pdl);
 }

@@ -86,6 +86,23 @@ size_t dfl2_last_error(char* buf, size_t len);
 /* Number of kernels this library has launched in this process (all devices). */
 uint64_t dfl2_launch_count(void);
 
+/* Engine of the projection GEMM (A = W_A E[a], B = W_B E[b], the gate's W_H h)
+ * on its split-K path, the one that runs when the rows are few (batch 1 on the
+ * drafter shapes: 241 + 256 gathered rows, 16 hidden rows); the batched path
+ * always uses tcgen05.
+ *   DFL2_PROJ_TENSOR (default): tcgen05 MMAs into a tensor-memory accumulator.
+ *   DFL2_PROJ_WARP: the warp-level engine, each warp owning 32 output columns of
+ *     its CTA's rows and computing them with mma.sync (m16n8k16, bf16 in, fp32
+ *     accumulate) from the same shared-memory tiles.  It applies where a CTA
+ *     holds 128 output columns (the batch-1 plans); elsewhere the tensor engine
+ *     runs.
+ * Process-wide (every device and thread), read when a call is enqueued; a
+ * captured CUDA graph keeps the engine it was captured with.  Returns the
+ * previous setting; an unknown value returns -1 and changes nothing. */
+#define DFL2_PROJ_TENSOR 0
+#define DFL2_PROJ_WARP 1
+int dfl2_set_projection_engine(int engine);
+
 /* Zero-fills a workspace on the stream (one cudaMemsetAsync). */
 dfl2_status dfl2_workspace_init(void* ws, size_t ws_bytes, dfl2_stream stream);
 

@@ -47,6 +47,18 @@ def test_version_and_counters(lib):
     assert dfl2.dfl2_launch_count() >= 0
 
 
+def test_projection_engine_switch(lib):
+    """The engine setter returns the previous engine and refuses unknown values."""
+    prev = lib.dfl2_set_projection_engine(dfl2.PROJ_WARP)
+    assert prev in (dfl2.PROJ_TENSOR, dfl2.PROJ_WARP)
+    assert lib.dfl2_set_projection_engine(dfl2.PROJ_TENSOR) == dfl2.PROJ_WARP
+    assert lib.dfl2_set_projection_engine(7) == -1
+    assert lib.dfl2_set_projection_engine(-1) == -1
+    assert lib.dfl2_set_projection_engine(prev) == dfl2.PROJ_TENSOR
+    with pytest.raises(ValueError):
+        dfl2.dfl2_set_projection_engine(3)
+
+
 def test_topk_rejects_bad_arguments(lib):
     ws = dfl2.dfl2_topk_workspace_size(1, 8, 1024)
     assert ws > 0
