@@ -510,10 +510,14 @@ def measure_e2e(case: Case, g_step, steps, warmup, flush):
     d2h = case.staged_out.nbytes
     stream = torch.cuda.current_stream()
     ts = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(warmup + steps)]
     for i in range(warmup + steps):
         flush.fill_(i & 0xFF)
-        torch.cuda._sleep(20000)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # the GPU sleeps while the host enqueues the copies and the replay, so that
+        # no host-side enqueue time falls inside the timed region
+        torch.cuda._sleep(200000)
+        a, b = ev[i]
         a.record(stream)
         case.staged_in.buf.copy_(pinned_in, non_blocking=True)
         g_step.replay()

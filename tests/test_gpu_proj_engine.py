@@ -74,3 +74,21 @@ def test_tail_warp_engine(T):
     inp = wl.make_tail_inputs(w, "cpu")
     with engine(dfl2.PROJ_WARP):
         check_tail(w, lg, inp, T, inp["seeds"], 5, [0])
+
+
+@pytest.mark.parametrize("name,B,L,V,d", [
+    ("drafter4b_l16", 3, 16, 151936, 2560),   # CTAs of 256 columns: the tcgen05 engine runs
+    ("tiny_l8_v32k", 1, 8, 32768, 1024),     # CTAs of 64 columns: the tcgen05 engine runs
+    ("tiny_l8_v32k", 40, 16, 4096, 256),     # the batched projection (no split K)
+])
+def test_warp_engine_request_elsewhere(name, B, L, V, d):
+    """Asking for the warp-level engine on a plan it does not apply to leaves
+    the scores exact to the usual tolerance."""
+    w = wl.WORKLOADS[name].with_(B=B, L=L, V=V, d=d, e_std=1.0)
+    inp = wl.make_tail_inputs(w, "cpu")
+    idx, val = candidates_from_oracle(wl.make_logits(w, "cpu"))
+    with engine(dfl2.PROJ_WARP):
+        S = gpu_select(idx, val, inp["verified"], inp)
+    seqs = list(range(min(B, 8)))
+    ref = oracle_select_subset(idx, val, inp["verified"], inp, seqs)
+    assert_scores_close(S[seqs], ref, f"warp engine requested, {name} B={B}")
