@@ -639,13 +639,79 @@ struct PairArgs {
 };
 
 // One CTA per (sequence b, position t), 128 threads.  The 16x16 dot products
-// of length 256 read shared memory 16 bytes at a time with 2x2 register
-// blocking: thread (half h, ip, jp) forms rows {ip, ip+8} x columns {jp, jp+8}
-// over half h of the rank, and the two halves are added at the end.  Rows sit
-// kPairPitch floats apart (16-byte aligned, and eight consecutive rows fall in
-// different bank groups).
+// of length 256 (bilinear16) read shared memory 16 bytes at a time into 4x4
+// register blocks.  Rows sit kPairPitch floats apart (16-byte aligned, and
+// eight consecutive rows fall in different bank groups).
 constexpr int kPairThreads = 128;
 constexpr int kPairPitch = kRank + 4;
+
+// The nearest tf32 value of x (10 explicit mantissa bits), in a 32-bit register.
+__device__ __forceinline__ uint32_t tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void mma_1688_tf32(float d[4], const uint32_t a[4], const uint32_t b[2]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+// out[i][j] = sum over the 256 ranks of Gs[i][q] * Bsh[j][q] for the 16 x 16
+// pairs, by the 128 threads of a group, on the tensor cores: warp w takes the
+// ranks [64 w, 64 w + 64) as eight k8 steps of m16n8k8 MMAs (M = the 16 rows i,
+// N = two tiles of 8 columns j), each operand read from shared memory once.
+// fp32 accuracy from tf32 MMAs: each value is split into its nearest tf32 and
+// the tf32 of the remainder, and a*b is taken as a_hi*b_lo + a_lo*b_hi +
+// a_hi*b_hi (the dropped a_lo*b_lo is below 2^-22 of |a*b|), accumulated in
+// fp32.  The four warps' partial tiles are added in warp order through the
+// bytes of Gs, which the products no longer need (so Gs is overwritten); the
+// caller synchronises the group before and after.
+template <typename Sync>
+__device__ __forceinline__ void bilinear16(float (*Gs)[kPairPitch], const float (*Bsh)[kPairPitch],
+                                           float (*out)[kCand + 1], int tid, Sync sync) {
+  const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 2
+  for (int ks = 0; ks < 8; ++ks) {
+    const int k0 = 64 * w + 8 * ks;
+    const float av[4] = {Gs[g][k0 + t], Gs[g + 8][k0 + t], Gs[g][k0 + t + 4], Gs[g + 8][k0 + t + 4]};
+    uint32_t ahi[4], alo[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      ahi[r] = tf32_rna(av[r]);
+      alo[r] = tf32_rna(av[r] - __uint_as_float(ahi[r]));
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float bv[2] = {Bsh[8 * nt + g][k0 + t], Bsh[8 * nt + g][k0 + t + 4]};
+      uint32_t bhi[2], blo[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        bhi[r] = tf32_rna(bv[r]);
+        blo[r] = tf32_rna(bv[r] - __uint_as_float(bhi[r]));
+      }
+      mma_1688_tf32(d[nt], ahi, blo);
+      mma_1688_tf32(d[nt], alo, bhi);
+      mma_1688_tf32(d[nt], ahi, bhi);
+    }
+  }
+  sync();  // every warp is past its last read of Gs
+  // d[nt]: (row g, columns 8 nt + 2t, +1) and (row g + 8, the same columns)
+  float* part = &Gs[0][0];  // 4 x 16 x 16 floats, within Gs's 16 x kPairPitch
+  float* pw = part + w * kCand * kCand;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    *reinterpret_cast<float2*>(pw + g * kCand + 8 * nt + 2 * t) = make_float2(d[nt][0], d[nt][1]);
+    *reinterpret_cast<float2*>(pw + (g + 8) * kCand + 8 * nt + 2 * t) = make_float2(d[nt][2], d[nt][3]);
+  }
+  sync();
+  for (int e = tid; e < kCand * kCand; e += kPairThreads)
+    out[e / kCand][e % kCand] = ((part[e] + part[kCand * kCand + e]) + part[2 * kCand * kCand + e]) +
+                                part[3 * kCand * kCand + e];
+}
 
 __global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
   __shared__ __align__(16) float Gs[kCand][kPairPitch];   // A(a_i) ⊙ H(h_t)
@@ -653,7 +719,6 @@ __global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
   __shared__ float Hs[kRank];
   __shared__ float U[kCand];
   __shared__ float Srow[kCand][kCand + 1];
-  __shared__ float Shalf[kCand][kCand + 1];  // the second rank half's partial sums
   __shared__ int path[128];
   __shared__ uint32_t last;
   pdl_wait();
@@ -716,37 +781,12 @@ __global__ void __launch_bounds__(kPairThreads) pair16_kernel(PairArgs a) {
     *reinterpret_cast<float4*>(&Bsh[i][c]) = vb[k];
   }
   __syncthreads();
-  {
-    const int half = tid >> 6, tt = tid & 63;
-    const int ip = tt >> 3, jp = tt & 7;
-    const int q0 = half * (kRank / 2);
-    float4 s00 = make_float4(0.f, 0.f, 0.f, 0.f), s01 = s00, s10 = s00, s11 = s00;
-#pragma unroll 4
-    for (int q = q0; q < q0 + kRank / 2; q += 4) {
-      const float4 g0 = *reinterpret_cast<const float4*>(&Gs[ip][q]);
-      const float4 g1 = *reinterpret_cast<const float4*>(&Gs[ip + 8][q]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&Bsh[jp][q]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&Bsh[jp + 8][q]);
-      s00.x = fmaf(g0.x, b0.x, s00.x); s00.y = fmaf(g0.y, b0.y, s00.y);
-      s00.z = fmaf(g0.z, b0.z, s00.z); s00.w = fmaf(g0.w, b0.w, s00.w);
-      s01.x = fmaf(g0.x, b1.x, s01.x); s01.y = fmaf(g0.y, b1.y, s01.y);
-      s01.z = fmaf(g0.z, b1.z, s01.z); s01.w = fmaf(g0.w, b1.w, s01.w);
-      s10.x = fmaf(g1.x, b0.x, s10.x); s10.y = fmaf(g1.y, b0.y, s10.y);
-      s10.z = fmaf(g1.z, b0.z, s10.z); s10.w = fmaf(g1.w, b0.w, s10.w);
-      s11.x = fmaf(g1.x, b1.x, s11.x); s11.y = fmaf(g1.y, b1.y, s11.y);
-      s11.z = fmaf(g1.z, b1.z, s11.z); s11.w = fmaf(g1.w, b1.w, s11.w);
-    }
-    float (*dst)[kCand + 1] = half ? Shalf : Srow;
-    dst[ip][jp] = (s00.x + s00.y) + (s00.z + s00.w);
-    dst[ip][jp + 8] = (s01.x + s01.y) + (s01.z + s01.w);
-    dst[ip + 8][jp] = (s10.x + s10.y) + (s10.z + s10.w);
-    dst[ip + 8][jp + 8] = (s11.x + s11.y) + (s11.z + s11.w);
-  }
+  bilinear16(Gs, Bsh, Srow, tid, [] { __syncthreads(); });
   __syncthreads();
-  // S = U_t(b_j) + the two rank halves; rows past the predecessors are -inf
+  // S = U_t(b_j) + the bilinear term; rows past the predecessors are -inf
   for (int e = tid; e < kCand * kCand; e += kPairThreads) {
     const int i = e / kCand, j = e % kCand;
-    const float v = i < npred ? (Srow[i][j] + Shalf[i][j]) + U[j] : -INFINITY;
+    const float v = i < npred ? Srow[i][j] + U[j] : -INFINITY;
     Srow[i][j] = v;
     a.scores[size_t(cell) * kCand * kCand + e] = v;
   }
@@ -826,7 +866,6 @@ struct PairGroupSmem {
   float Hs[kRank];
   float U[kCand];
   float Srow[kCand][kCand + 1];
-  float Shalf[kCand][kCand + 1];
   const float* rowA[kCand];
   const float* rowB[kCand];
 };
@@ -922,36 +961,11 @@ __device__ __forceinline__ void pair_position(const PairArgs& a, int b, int t, i
     *reinterpret_cast<float4*>(&g->Bsh[i][c]) = vb[k];
   }
   sync();
-  {
-    const int half = tid >> 6, tt = tid & 63;
-    const int ip = tt >> 3, jp = tt & 7;
-    const int q0 = half * (kRank / 2);
-    float4 s00 = make_float4(0.f, 0.f, 0.f, 0.f), s01 = s00, s10 = s00, s11 = s00;
-#pragma unroll 4
-    for (int q = q0; q < q0 + kRank / 2; q += 4) {
-      const float4 g0 = *reinterpret_cast<const float4*>(&g->Gs[ip][q]);
-      const float4 g1 = *reinterpret_cast<const float4*>(&g->Gs[ip + 8][q]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&g->Bsh[jp][q]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&g->Bsh[jp + 8][q]);
-      s00.x = fmaf(g0.x, b0.x, s00.x); s00.y = fmaf(g0.y, b0.y, s00.y);
-      s00.z = fmaf(g0.z, b0.z, s00.z); s00.w = fmaf(g0.w, b0.w, s00.w);
-      s01.x = fmaf(g0.x, b1.x, s01.x); s01.y = fmaf(g0.y, b1.y, s01.y);
-      s01.z = fmaf(g0.z, b1.z, s01.z); s01.w = fmaf(g0.w, b1.w, s01.w);
-      s10.x = fmaf(g1.x, b0.x, s10.x); s10.y = fmaf(g1.y, b0.y, s10.y);
-      s10.z = fmaf(g1.z, b0.z, s10.z); s10.w = fmaf(g1.w, b0.w, s10.w);
-      s11.x = fmaf(g1.x, b1.x, s11.x); s11.y = fmaf(g1.y, b1.y, s11.y);
-      s11.z = fmaf(g1.z, b1.z, s11.z); s11.w = fmaf(g1.w, b1.w, s11.w);
-    }
-    float (*dst)[kCand + 1] = half ? g->Shalf : g->Srow;
-    dst[ip][jp] = (s00.x + s00.y) + (s00.z + s00.w);
-    dst[ip][jp + 8] = (s01.x + s01.y) + (s01.z + s01.w);
-    dst[ip + 8][jp] = (s10.x + s10.y) + (s10.z + s10.w);
-    dst[ip + 8][jp + 8] = (s11.x + s11.y) + (s11.z + s11.w);
-  }
+  bilinear16(g->Gs, g->Bsh, g->Srow, tid, sync);
   sync();
   for (int e = tid; e < kCand * kCand; e += kPairThreads) {
     const int i = e / kCand, j = e % kCand;
-    const float v = i < npred ? (g->Srow[i][j] + g->Shalf[i][j]) + g->U[j] : -INFINITY;
+    const float v = i < npred ? g->Srow[i][j] + g->U[j] : -INFINITY;
     g->Srow[i][j] = v;
     if (a.scores) a.scores[size_t(cell) * kCand * kCand + e] = v;
   }
@@ -981,10 +995,13 @@ __global__ void __launch_bounds__(kPairThreads * P) pair_walk_kernel(PairArgs a)
     cluster_arrive_release();  // the first CTA's barrier is initialised before any store
   else
     __syncthreads();
+  // The walk's random number for this position, before the dependency wait:
+  // the Philox keys are the caller's input, and this kernel only starts once
+  // the kernel before it has passed its own wait (so everything the caller
+  // queued before this library's calls has finished).
+  const float u = live && a.T > 0.f ? walk_uniform(__ldcg(a.seeds + b), a.cycle, t) : 0.f;
   pdl_wait();
   pdl_launch_dependents();
-  // the walk's random number for this position, in flight during the scores
-  const float u = live && a.T > 0.f ? walk_uniform(__ldcg(a.seeds + b), a.cycle, t) : 0.f;
   auto sync = [grp]() { named_sync(1 + grp, kPairThreads); };
   if (live) pair_position(a, b, t, tid, g, sync);
   // ---- the walk's decision for every predecessor row of position t, and the
