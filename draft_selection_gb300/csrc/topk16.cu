@@ -683,25 +683,29 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
 //     distributed shared memory and arrive on its mbarrier; it ranks the C
 //     lists by binary search in each.  No global atomics or fences.
 // ============================================================================
-constexpr int kRStages = 8;
+constexpr int kRStages = 8;       // clusters of C > 1 CTAs per row (few tiles per CTA)
+constexpr int kRStagesRow = 12;   // one CTA per row (a whole row streams through the ring)
 constexpr int kRMaxCluster = 8;
 constexpr int kRMaxTilesPerCta = 16;
 constexpr int kRCandCap = 1024;
 // Shared memory: [stages][full][empty][list barrier, pad][cand][extra][res]
 // [cluster lists][lane maxima][their top 16][flags]; every region after the
 // barriers starts on a 16-byte boundary (the lists are read 16 bytes at a time).
-constexpr size_t kROffBars = size_t(kRStages) * kTileBytes;
-constexpr size_t kROffCand = kROffBars + (2 * kRStages + 2) * sizeof(uint64_t);
-constexpr size_t kROffExtra = kROffCand + size_t(kRCandCap) * sizeof(uint64_t);
-constexpr size_t kROffRes = kROffExtra + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
-constexpr size_t kROffClists = kROffRes + kCand * sizeof(uint64_t);
-constexpr size_t kROffWsorted = kROffClists + size_t(kRMaxCluster) * kCand * sizeof(uint64_t);
-constexpr size_t kROffTres = kROffWsorted + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
-constexpr size_t kROffFlags = kROffTres + kCand * sizeof(uint64_t);
-constexpr size_t kRSmemBytes = kROffFlags + 16;
-static_assert(kROffCand % 16 == 0 && kROffExtra % 16 == 0 && kROffRes % 16 == 0 &&
-                  kROffClists % 16 == 0 && kROffWsorted % 16 == 0 && kROffTres % 16 == 0,
-              "16-byte aligned regions");
+template <int NST>
+struct RowsLayout {
+  static constexpr size_t bars = size_t(NST) * kTileBytes;
+  static constexpr size_t cand = bars + (2 * NST + 2) * sizeof(uint64_t);
+  static constexpr size_t extra = cand + size_t(kRCandCap) * sizeof(uint64_t);
+  static constexpr size_t res = extra + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
+  static constexpr size_t clists = res + kCand * sizeof(uint64_t);
+  static constexpr size_t wsorted = clists + size_t(kRMaxCluster) * kCand * sizeof(uint64_t);
+  static constexpr size_t tres = wsorted + size_t(kConsumerWarps) * kCand * sizeof(uint64_t);
+  static constexpr size_t flags = tres + kCand * sizeof(uint64_t);
+  static constexpr size_t bytes = flags + 16;
+  static_assert(cand % 16 == 0 && extra % 16 == 0 && res % 16 == 0 && clists % 16 == 0 &&
+                    wsorted % 16 == 0 && tres % 16 == 0,
+                "16-byte aligned regions");
+};
 static_assert(kConsumerWarps <= kRMaxCluster, "lists ranked by rank_sorted_lists16");
 
 struct RowsArgs {
@@ -836,20 +840,21 @@ __device__ __forceinline__ void rank_lists16(const uint64_t* lists, int n, uint6
   if (r < kCand) res[r] = v;
 }
 
-template <int EPV>
+template <int EPV, int NST>
 __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
+  using Lay = RowsLayout<NST>;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
-  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kROffBars);
-  uint64_t* empty_bar = full_bar + kRStages;
-  uint64_t* list_bar = empty_bar + kRStages;  // first CTA: the others' lists arrived
-  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + kROffCand);       // [kRCandCap]
-  uint64_t* extra = reinterpret_cast<uint64_t*>(smem + kROffExtra);     // [kConsumerWarps][16]
-  uint64_t* res = reinterpret_cast<uint64_t*>(smem + kROffRes);         // [16]
-  uint64_t* clists = reinterpret_cast<uint64_t*>(smem + kROffClists);   // [kRMaxCluster][16]
-  uint64_t* wsorted = reinterpret_cast<uint64_t*>(smem + kROffWsorted); // [warps][16] lane maxima
-  uint64_t* tres = reinterpret_cast<uint64_t*>(smem + kROffTres);       // [16] their top 16
-  uint32_t* cand_count = reinterpret_cast<uint32_t*>(smem + kROffFlags);
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::bars);
+  uint64_t* empty_bar = full_bar + NST;
+  uint64_t* list_bar = empty_bar + NST;  // first CTA: the others' lists arrived
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + Lay::cand);       // [kRCandCap]
+  uint64_t* extra = reinterpret_cast<uint64_t*>(smem + Lay::extra);     // [kConsumerWarps][16]
+  uint64_t* res = reinterpret_cast<uint64_t*>(smem + Lay::res);         // [16]
+  uint64_t* clists = reinterpret_cast<uint64_t*>(smem + Lay::clists);   // [kRMaxCluster][16]
+  uint64_t* wsorted = reinterpret_cast<uint64_t*>(smem + Lay::wsorted); // [warps][16] lane maxima
+  uint64_t* tres = reinterpret_cast<uint64_t*>(smem + Lay::tres);       // [16] their top 16
+  uint32_t* cand_count = reinterpret_cast<uint32_t*>(smem + Lay::flags);
   uint32_t* issued = cand_count + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -863,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   const RowWin win = row_window(row, row_bytes, floor16);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kRStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -884,14 +889,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   if (warp == kConsumerWarps) {  // producer
     if (lane == 0) {
       for (int i = 0, s = 0, ph = 0; i < n; ++i) {
-        if (i >= kRStages && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
+        if (i >= NST && !mbar_wait(&empty_bar[s], ph ^ 1, a.err)) record_error(a.err, kDevErrTopkEmpty);
         const uint32_t bytes = tile_bytes(win, t_lo + i);
         mbar_arrive_expect_tx(&full_bar[s], bytes);
         if (bytes)
           bulk_g2s(stages + size_t(s) * kTileBytes,
                    a.logits + win.lo + size_t(t_lo + i) * kTileBytes, bytes, &full_bar[s]);
         st_release_cta(issued, static_cast<uint32_t>(i + 1));
-        if (++s == kRStages) {
+        if (++s == NST) {
           s = 0;
           ph ^= 1;
         }
@@ -901,9 +906,9 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   } else {
     // Warp w scans tiles w, w + 8, ...: each stage serves one warp only.
     auto stage_of = [&](int i, const uint4*& tile, int& nvec, uint32_t& eb) {
-      const int st = i % kRStages;
+      const int st = i % NST;
       if (!wait_count_above(issued, static_cast<uint32_t>(i), a.err) ||
-          !mbar_wait(&full_bar[st], (i / kRStages) & 1, a.err))
+          !mbar_wait(&full_bar[st], (i / NST) & 1, a.err))
         record_error(a.err, kDevErrTopkFull);
       const int t = t_lo + i;
       nvec = finish_tile<EPV>(stages + size_t(st) * kTileBytes, t, win, floor16, a.logits, lane);
@@ -962,7 +967,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
         append_tile_keys<EPV>(w, tile, nvec, eb, vmh, T, bval, lk, lane, cand + kCand, cand_count);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[i % kRStages]);
+      if (lane == 0) mbar_arrive(&empty_bar[i % NST]);
     }
     if (lane < kCand) extra[warp * kCand + lane] = w.list;
     named_sync(1, kConsumers);
@@ -1025,11 +1030,21 @@ cudaError_t ensure_setup(int dev, KernelSetup*& out) {
     e = cudaFuncSetAttribute(topk16_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk16_rows_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kRSmemBytes));
+    e = cudaFuncSetAttribute(topk16_rows_kernel<4, kRStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStages>::bytes));
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk16_rows_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kRSmemBytes));
+    e = cudaFuncSetAttribute(topk16_rows_kernel<8, kRStages>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStages>::bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_rows_kernel<4, kRStagesRow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStagesRow>::bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_rows_kernel<8, kRStagesRow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStagesRow>::bytes));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k.occ4, topk16_kernel<4>, kThreads,
                                                       kSmemBytes);
@@ -1076,12 +1091,21 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
   if (e != cudaSuccess) return e;
   const DeviceInfo info = device_info();
   // Few rows: one cluster of C CTAs per row while the clusters fit in about one
-  // wave (two CTAs per SM) and each CTA streams at most kRMaxTilesPerCta tiles.
+  // wave (two CTAs per SM) and each CTA streams at most kRMaxTilesPerCta tiles
+  // (ring of kRStages).  Rows enough to give every SM a CTA: one CTA per row,
+  // each streaming its whole row through a deeper ring, in as many waves as it
+  // takes (serving_b64, 1,024 rows: 74 us against 91 for the persistent
+  // kernel, whose row segments, bound phases and cross-CTA merges stall its
+  // rings).  Otherwise (few rows of many tiles) the persistent kernel spreads
+  // the tiles over the whole GPU.
   {
     int C = std::min(kRMaxCluster, plan.tiles_per_row);
     while (C > 1 && (long long)plan.rows * C > 2LL * info.sms) C >>= 1;
-    if ((long long)plan.rows * C <= 2LL * info.sms &&
-        (plan.tiles_per_row + C - 1) / C <= kRMaxTilesPerCta) {
+    const bool clusters = (long long)plan.rows * C <= 2LL * info.sms &&
+                          (plan.tiles_per_row + C - 1) / C <= kRMaxTilesPerCta;
+    const bool per_row = !clusters && plan.rows >= info.sms;
+    if (clusters || per_row) {
+      if (per_row) C = 1;
       RowsArgs r;
       r.logits = static_cast<const uint8_t*>(logits);
       r.V = plan.V;
@@ -1092,9 +1116,16 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
       r.out_val = val;
       r.err = device_error_word();
       const dim3 grid(static_cast<unsigned>(plan.rows * C));
+      if (per_row) {
+        constexpr size_t smem = RowsLayout<kRStagesRow>::bytes;
+        if (plan.elem_bytes == 4)
+          return launch_kc(topk16_rows_kernel<4, kRStagesRow>, grid, dim3(kThreads), smem, s, pdl, 1, r);
+        return launch_kc(topk16_rows_kernel<8, kRStagesRow>, grid, dim3(kThreads), smem, s, pdl, 1, r);
+      }
+      constexpr size_t smem = RowsLayout<kRStages>::bytes;
       if (plan.elem_bytes == 4)
-        return launch_kc(topk16_rows_kernel<4>, grid, dim3(kThreads), kRSmemBytes, s, pdl, C, r);
-      return launch_kc(topk16_rows_kernel<8>, grid, dim3(kThreads), kRSmemBytes, s, pdl, C, r);
+        return launch_kc(topk16_rows_kernel<4, kRStages>, grid, dim3(kThreads), smem, s, pdl, C, r);
+      return launch_kc(topk16_rows_kernel<8, kRStages>, grid, dim3(kThreads), smem, s, pdl, C, r);
     }
   }
   const int occ = plan.elem_bytes == 4 ? k->occ4 : k->occ2;

@@ -140,13 +140,15 @@ def test_edge_shapes(B, L, V, dt):
 
 @pytest.mark.parametrize("B,L,V,dt", [
     (1, 7, 50257, torch.bfloat16),   # rows start anywhere in a 16-byte unit: cluster kernel
-    (64, 16, 50257, torch.bfloat16),  # the same, rows split across CTAs: persistent kernel
+    (64, 16, 50257, torch.bfloat16),  # the same, one CTA per row
     (3, 5, 1021, torch.float32),     # float32 rows of an odd length
-    (40, 16, 1023, torch.float32),   # many short odd rows (several per CTA)
+    (40, 16, 1023, torch.float32),   # many short odd rows
     (1, 3, 17, torch.bfloat16),      # one past the minimum: rows of 34 bytes
     (5, 3, 4099, torch.bfloat16),    # the buffer ends 10 bytes past its last whole 16
-    (37, 9, 1023, torch.float32),    # the same in the persistent kernel (float32)
+    (37, 9, 1023, torch.float32),    # the same, one CTA per row (float32)
     (63, 5, 50257, torch.bfloat16),  # and bf16
+    (2, 8, 1000003, torch.bfloat16),  # few long rows split across CTAs: persistent kernel
+    (1, 5, 500009, torch.float32),   # the same in float32
 ])
 def test_unaligned_rows(B, L, V, dt):
     """Rows whose start is not a multiple of 16 bytes: each is streamed as the

@@ -44,31 +44,36 @@ def without_workspace(lg):
 def _persistent_split_path(B, L, V):
     """True when dfl2_topk runs its persistent kernel for this shape, where rows
     are split across CTAs and the partial lists and per-row tickets live in the
-    scratch: the cluster-per-row kernel (few rows) uses no scratch at all.  The
-    rule restates the library's dispatch: one cluster of C <= 8 CTAs per row
-    while rows * C <= 2 * SMs and each CTA streams at most 16 tiles of 8 KB."""
+    scratch; the row kernels (one cluster, or one CTA, per row) use no scratch.
+    The rule restates the library's dispatch: one cluster of C <= 8 CTAs per row
+    while rows * C <= 2 * SMs and each CTA streams at most 16 tiles of 8 KB;
+    otherwise one CTA per row once there are at least as many rows as SMs;
+    otherwise the persistent kernel."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rows = B * L
     tiles = -(-V * 2 // 8192)  # bf16 rows
     C = min(8, tiles)
-    while C > 1 and B * L * C > 2 * sms:
+    while C > 1 and rows * C > 2 * sms:
         C //= 2
-    return not (B * L * C <= 2 * sms and -(-tiles // C) <= 16)
+    clusters = rows * C <= 2 * sms and -(-tiles // C) <= 16
+    return not clusters and rows < sms
 
 
 def test_matches_dfl2_topk_on_calls_in_a_row():
-    # Two calls in a row on a shape whose rows are split across CTAs (the
-    # scratch's partial lists and tickets are used; the second call reuses the
-    # tickets the first one left), then a shape with four times the rows (a
-    # different ticket and partial-list layout in the same array), then the
-    # batch-1 4B-drafter block, which takes the scratch-free cluster kernel.
-    base = wl.WORKLOADS["serving_b64"]
-    split16 = base.with_(B=16)
-    split64 = base
-    for w in (split16, split64):
+    # Two calls in a row on a shape whose rows are split across CTAs (few rows of
+    # a 524,288-entry vocabulary: the scratch's partial lists and tickets are
+    # used; the second call reuses the tickets the first one left), then a shape
+    # with twice the rows (a different ticket and partial-list layout in the
+    # same array), then the batch-1 4B-drafter block, which takes the
+    # scratch-free cluster kernel.
+    base = wl.WORKLOADS["serving_b64"].with_(V=524288)
+    split_a = base.with_(B=4)
+    split_b = base.with_(B=8, seed=2003)
+    for w in (split_a, split_b):
         assert _persistent_split_path(w.B, w.L, w.V), w
         assert dfl2.dfl2_topk_workspace_size(w.B, w.L, w.V) <= 4 << 20
-    first = wl.make_logits(split16, "cuda")
-    second = wl.make_logits(split64.with_(seed=2003), "cuda")
+    first = wl.make_logits(split_a, "cuda")
+    second = wl.make_logits(split_b, "cuda")
     third = wl.make_logits(wl.WORKLOADS["drafter4b_l16"], "cpu").cuda()
     got = [without_workspace(first), without_workspace(first), without_workspace(second),
            without_workspace(third)]
