@@ -685,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 3) topk16_kernel(TopkArgs a) {
 // ============================================================================
 constexpr int kRStages = 8;       // clusters of C > 1 CTAs per row (few tiles per CTA)
 constexpr int kRStagesRow = 12;   // one CTA per row (a whole row streams through the ring)
+constexpr int kRowLoopCtasPerSm = 2;  // resident CTAs of the row-looping kernel per SM
 constexpr int kRMaxCluster = 8;
 constexpr int kRMaxTilesPerCta = 16;
 constexpr int kRCandCap = 1024;
@@ -1014,6 +1015,167 @@ __global__ void __launch_bounds__(kThreads, 2) topk16_rows_kernel(RowsArgs a) {
   pdl_launch_dependents();
 }
 
+// One CTA per row, persistent over rows: CTA c takes rows c, c + G, c + 2G, ...
+// (G = gridDim.x) and its producer streams their tiles back to back through the
+// ring, so the next row's first tiles arrive while the consumers rank the
+// current one.  Per row, the same steps as the cluster kernel with C = 1: the
+// bound from the first wave of tiles, every element at or above it appended,
+// the top 16 by rank.  Tile i of the CTA (counted over its rows) sits in stage
+// i % NST; a consumer waits for the producer to have issued it before the
+// stage's parity (the producer may be a whole ring ahead).
+template <int EPV, int NST>
+__global__ void __launch_bounds__(kThreads, 2) topk16_row_loop_kernel(RowsArgs a) {
+  using Lay = RowsLayout<NST>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + Lay::bars);
+  uint64_t* empty_bar = full_bar + NST;
+  uint64_t* cand = reinterpret_cast<uint64_t*>(smem + Lay::cand);       // [kRCandCap]
+  uint64_t* extra = reinterpret_cast<uint64_t*>(smem + Lay::extra);     // [kConsumerWarps][16]
+  uint64_t* res = reinterpret_cast<uint64_t*>(smem + Lay::res);         // [16]
+  uint64_t* wsorted = reinterpret_cast<uint64_t*>(smem + Lay::wsorted); // [warps][16] lane maxima
+  uint64_t* tres = reinterpret_cast<uint64_t*>(smem + Lay::tres);       // [16] their top 16
+  uint32_t* cand_count = reinterpret_cast<uint32_t*>(smem + Lay::flags);
+  uint32_t* issued = cand_count + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long G = gridDim.x;
+  const int n = a.tiles_per_row;
+  const size_t row_bytes = size_t(a.V) * (16 / EPV);
+  const size_t floor16 = (size_t(a.rows) * row_bytes) & ~size_t(15);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NST; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    fence_mbar_init();
+    *issued = 0u;
+    *cand_count = 0u;
+  }
+  if (threadIdx.x < kCand) {
+    res[threadIdx.x] = 0ull;
+    tres[threadIdx.x] = 0ull;
+  }
+  if (threadIdx.x < kConsumerWarps * kCand) wsorted[threadIdx.x] = 0ull;
+  __syncthreads();
+  pdl_wait();  // the logits may come from the previous kernel on the stream
+
+  if (warp == kConsumerWarps) {  // producer
+    if (lane == 0) {
+      uint32_t i = 0;
+      int s = 0, ph = 0;
+      for (long long row = blockIdx.x; row < a.rows; row += G) {
+        const RowWin win = row_window(row, row_bytes, floor16);
+        for (int t = 0; t < n; ++t, ++i) {
+          if (i >= uint32_t(NST) && !mbar_wait(&empty_bar[s], ph ^ 1, a.err))
+            record_error(a.err, kDevErrTopkEmpty);
+          const uint32_t bytes = tile_bytes(win, t);
+          mbar_arrive_expect_tx(&full_bar[s], bytes);
+          if (bytes)
+            bulk_g2s(stages + size_t(s) * kTileBytes, a.logits + win.lo + size_t(t) * kTileBytes,
+                     bytes, &full_bar[s]);
+          st_release_cta(issued, i + 1);
+          if (++s == NST) {
+            s = 0;
+            ph ^= 1;
+          }
+        }
+      }
+    }
+  } else {
+    uint32_t base = 0;  // CTA tile index of the row's first tile
+    for (long long row = blockIdx.x; row < a.rows; row += G, base += uint32_t(n)) {
+      const RowWin win = row_window(row, row_bytes, floor16);
+      auto stage_of = [&](int j, const uint4*& tile, int& nvec, uint32_t& eb) {
+        const uint32_t i = base + uint32_t(j);
+        const int st = int(i % NST);
+        if (!wait_count_above(issued, i, a.err) || !mbar_wait(&full_bar[st], (i / NST) & 1, a.err))
+          record_error(a.err, kDevErrTopkFull);
+        nvec = finish_tile<EPV>(stages + size_t(st) * kTileBytes, j, win, floor16, a.logits, lane);
+        eb = tile_ebase<EPV>(win, j);
+        tile = reinterpret_cast<const uint4*>(stages + size_t(st) * kTileBytes);
+      };
+      WarpTop w{0ull, -INFINITY};
+      float vm[kVecPerLane];
+      const uint4* tile = nullptr;
+      int nvec = 0;
+      uint32_t eb = 0;
+      // ---- the bound T over the row's first wave of tiles (as in the cluster kernel) ----
+      uint64_t lk = 0ull;
+      if (warp < n) {
+        stage_of(warp, tile, nvec, eb);
+        lk = lane_max_key<EPV>(tile, nvec, eb, lane, vm);
+      }
+      {
+        int r = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r += shfl64(lk, j) > lk;
+        if (r < kCand && lk != 0ull) wsorted[warp * kCand + r] = lk;
+      }
+      const int nw = n < kConsumerWarps ? n : kConsumerWarps;
+      named_sync(1, kConsumers);
+      rank_lists16(wsorted, nw, tres, threadIdx.x);
+      named_sync(1, kConsumers);
+      const uint64_t T = tres[kCand - 1];  // 0 (fewer than 16 keys): accept all
+      const float bval = T ? unord_f32(static_cast<uint32_t>(T >> 32)) : -INFINITY;
+      if (threadIdx.x < kCand) cand[threadIdx.x] = T ? tres[threadIdx.x] : 0ull;
+      for (int j = warp; j < n; j += kConsumerWarps) {
+        if (j != warp) {
+          stage_of(j, tile, nvec, eb);
+#pragma unroll
+          for (int q = 0; q < kVecPerLane; ++q) {
+            const int v = lane + 32 * q;
+            vm[q] = v < nvec ? vec_max<EPV>(tile[v]) : -INFINITY;
+          }
+          append_tile_keys<EPV>(w, tile, nvec, eb, vm, T, bval, 0ull, lane, cand + kCand,
+                                cand_count);
+        } else if (T == 0ull) {
+          append_tile_keys<EPV>(w, tile, nvec, eb, vm, 0ull, -INFINITY, 0ull, lane, cand + kCand,
+                                cand_count);
+        } else {
+          const bool holds = lk >= T;
+          float vmh[kVecPerLane];
+#pragma unroll
+          for (int q = 0; q < kVecPerLane; ++q) vmh[q] = holds ? vm[q] : -INFINITY;
+          append_tile_keys<EPV>(w, tile, nvec, eb, vmh, T, bval, lk, lane, cand + kCand,
+                                cand_count);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[(base + uint32_t(j)) % NST]);
+      }
+      if (lane < kCand) extra[warp * kCand + lane] = w.list;
+      named_sync(1, kConsumers);
+      const uint32_t cnt = *reinterpret_cast<volatile uint32_t*>(cand_count);
+      if (cnt == 0u && T != 0ull) {
+        if (threadIdx.x < kCand) res[threadIdx.x] = tres[threadIdx.x];  // already in rank order
+      } else {
+        rank_select16(cand, cnt > static_cast<uint32_t>(kRCandCap - kCand)
+                                ? kRCandCap + kConsumerWarps * kCand
+                                : kCand + static_cast<int>(cnt),
+                      res, threadIdx.x);
+      }
+      named_sync(1, kConsumers);
+      if (threadIdx.x < kCand) {
+        const uint64_t key = res[threadIdx.x];
+        a.out_idx[row * kCand + threadIdx.x] = static_cast<int32_t>(~static_cast<uint32_t>(key));
+        a.out_val[row * kCand + threadIdx.x] = unord_f32(static_cast<uint32_t>(key >> 32));
+      }
+      named_sync(1, kConsumers);  // every read of this row's lists is done
+      // the next row starts from empty lists (the candidate slots it ranks are
+      // the ones it writes: below its own count, or all of them on overflow)
+      if (threadIdx.x < kCand) {
+        res[threadIdx.x] = 0ull;
+        tres[threadIdx.x] = 0ull;
+      }
+      if (threadIdx.x < kConsumerWarps * kCand) wsorted[threadIdx.x] = 0ull;
+      if (threadIdx.x == 0) *cand_count = 0u;
+      named_sync(1, kConsumers);
+    }
+  }
+  pdl_launch_dependents();
+}
+
 struct KernelSetup {
   bool done = false;
   int occ4 = 1, occ2 = 1;
@@ -1043,6 +1205,14 @@ cudaError_t ensure_setup(int dev, KernelSetup*& out) {
                              static_cast<int>(RowsLayout<kRStagesRow>::bytes));
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(topk16_rows_kernel<8, kRStagesRow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStagesRow>::bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_row_loop_kernel<4, kRStagesRow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(RowsLayout<kRStagesRow>::bytes));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk16_row_loop_kernel<8, kRStagesRow>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(RowsLayout<kRStagesRow>::bytes));
     if (e != cudaSuccess) return e;
@@ -1118,9 +1288,15 @@ cudaError_t launch_topk(const TopkPlan& plan, const void* logits, int32_t* idx, 
       const dim3 grid(static_cast<unsigned>(plan.rows * C));
       if (per_row) {
         constexpr size_t smem = RowsLayout<kRStagesRow>::bytes;
+        // the fewest rows per CTA that fit the resident CTAs, spread evenly
+        // (serving_b64: 4 rows on each of 256 CTAs measured 72.4 us, against
+        // 73.4 for 304 CTAs of 3-4 rows and 73.7 for one row per CTA)
+        const long long slots = kRowLoopCtasPerSm * (long long)info.sms;
+        const long long per = (plan.rows + slots - 1) / slots;
+        const dim3 lgrid(static_cast<unsigned>((plan.rows + per - 1) / per));
         if (plan.elem_bytes == 4)
-          return launch_kc(topk16_rows_kernel<4, kRStagesRow>, grid, dim3(kThreads), smem, s, pdl, 1, r);
-        return launch_kc(topk16_rows_kernel<8, kRStagesRow>, grid, dim3(kThreads), smem, s, pdl, 1, r);
+          return launch_k(topk16_row_loop_kernel<4, kRStagesRow>, lgrid, dim3(kThreads), smem, s, pdl, r);
+        return launch_k(topk16_row_loop_kernel<8, kRStagesRow>, lgrid, dim3(kThreads), smem, s, pdl, r);
       }
       constexpr size_t smem = RowsLayout<kRStages>::bytes;
       if (plan.elem_bytes == 4)
