@@ -149,6 +149,8 @@ def test_edge_shapes(B, L, V, dt):
     (63, 5, 50257, torch.bfloat16),  # and bf16
     (2, 8, 1000003, torch.bfloat16),  # few long rows split across CTAs: persistent kernel
     (1, 5, 500009, torch.float32),   # the same in float32
+    (20, 8, 16, torch.bfloat16),     # many rows of the minimum length, one CTA per row
+    (200, 1, 17, torch.float32),     # many 68-byte rows, several in each 16-byte-aligned window
 ])
 def test_unaligned_rows(B, L, V, dt):
     """Rows whose start is not a multiple of 16 bytes: each is streamed as the
