@@ -948,6 +948,14 @@ bool use_ptile(int R, int d, const PtilePlan& pl, int sms) {
 // (cp.async), so no CTA-wide barrier sits between the wait and the MMAs; the
 // mixing threads load their x_t and x_{t-1} at the same time.
 constexpr int kGvThreads = 256;  // 8 warps
+// x pieces (16 bytes) of a lane whose addresses are computed before the
+// dependency wait: 16 rows x 2 pieces per K step x up to 6 K steps per warp,
+// over 32 lanes (K slices of up to 6 x 8 x 16 = 768: d <= 6144 with clusters of
+// 8); a lane with more pieces computes the rest after the wait
+constexpr int kGvMaxPieces = 6;
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 constexpr int kGvWarps = kGvThreads / 32;
 constexpr int kGvMaxR = 16;      // positions = the MMA's 16 rows
 constexpr size_t kGvSmemMax = 200 * 1024;
@@ -1045,26 +1053,53 @@ __global__ void __launch_bounds__(kGvThreads) conv_gemv_kernel(const ConvGemvArg
       b1[h] = __ldg(reinterpret_cast<const float4*>(a.base + d + cmix) + h);
     }
   }
+  // The addresses the steps after the wait use, computed before it (integer
+  // divisions among them): the mix's x_t and x_{t-1} rows, and this lane's
+  // first kGvMaxPieces pieces of the warp's K steps of every x row.
+  const uint4* xt_src = nullptr;
+  const uint4* xm_src = nullptr;
+  if (mixer) {
+    const int t = p_mix % a.L;
+    xt_src = reinterpret_cast<const uint4*>(a.x + size_t(p_mix) * d + cmix);
+    xm_src = reinterpret_cast<const uint4*>(
+        (t > 0 ? a.x + size_t(p_mix - 1) * d : a.x_prev + size_t(p_mix / a.L) * d) + cmix);
+  }
+  const int steps = ks / 16;
+  const int s0 = warp * steps / kGvWarps, s1 = (warp + 1) * steps / kGvWarps;
+  const int per_row = (s1 - s0) * 2;  // 16-byte pieces of one x row
+  int npieces = 0;
+  uint32_t piece_dst[kGvMaxPieces];
+  const __nv_bfloat16* piece_src[kGvMaxPieces];
+#pragma unroll
+  for (int q = 0; q < kGvMaxPieces; ++q) {
+    const int e = lane + 32 * q;
+    piece_dst[q] = 0u;
+    piece_src[q] = a.x;
+    if (e < R * per_row) {
+      const int p = e / per_row, c = s0 * 16 + (e % per_row) * 8;
+      piece_dst[q] = smem_u32(xs + size_t(p) * pitch + 2 * c);
+      piece_src[q] = a.x + size_t(p) * d + k0 + c;
+      npieces = q + 1;
+    }
+  }
   if constexpr (C > 1) cluster_arrive_release();  // barrier inits visible to the peers
   pdl_wait();
 
   // ---- the mix's operands, in flight during the MMAs ----
   uint4 xt = make_uint4(0u, 0u, 0u, 0u), xm = xt;
   if (mixer) {
-    const int t = p_mix % a.L;
-    xt = __ldcg(reinterpret_cast<const uint4*>(a.x + size_t(p_mix) * d + cmix));
-    xm = __ldcg(reinterpret_cast<const uint4*>(
-        (t > 0 ? a.x + size_t(p_mix - 1) * d : a.x_prev + size_t(p_mix / a.L) * d) + cmix));
+    xt = __ldcg(xt_src);
+    xm = __ldcg(xm_src);
   }
   // ---- partial corrections: this warp's K steps of x_slice (16 x K) * W_slice^T ----
-  const int steps = ks / 16;
-  const int s0 = warp * steps / kGvWarps, s1 = (warp + 1) * steps / kGvWarps;
   float acc[NT][4];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
   if (s0 < s1) {
-    const int per_row = (s1 - s0) * 2;  // 16-byte pieces of one x row
-    for (int e = lane; e < R * per_row; e += 32) {
+#pragma unroll
+    for (int q = 0; q < kGvMaxPieces; ++q)
+      if (q < npieces) cp_async16_s(piece_dst[q], piece_src[q]);
+    for (int e = lane + 32 * kGvMaxPieces; e < R * per_row; e += 32) {  // wide K slices only
       const int p = e / per_row, c = s0 * 16 + (e % per_row) * 8;
       cp_async16(xs + size_t(p) * pitch + 2 * c, a.x + size_t(p) * d + k0 + c, true);
     }
