@@ -75,27 +75,37 @@ struct GemmArgs {
   uint32_t* err;
 };
 
-// Source row of A for row m of a problem, or nullptr (zero row).
-__device__ __forceinline__ const __nv_bfloat16* a_row(const GemmArgs& a, int kind, int m, int M) {
-  if (m >= M) return nullptr;
-  if (kind == kRowsHidden) return a.hidden + size_t(m) * a.d;
-  if (kind == kRowsE) return a.E + size_t(m) * a.d;  // the table build: every row of E in order
-  int32_t tok;
+// Where row m of a problem comes from, known before the dependency wait (only
+// the index arithmetic): direct rows (hidden states, E in order) as `row`, a
+// gathered row as the address of its token (the verified token or a
+// candidate, read after the wait), nothing past M.
+struct RowRef {
+  const __nv_bfloat16* row;
+  const int32_t* tok;
+};
+__device__ __forceinline__ RowRef a_row_ref(const GemmArgs& a, int kind, int m, int M) {
+  if (m >= M) return RowRef{nullptr, nullptr};
+  if (kind == kRowsHidden) return RowRef{a.hidden + size_t(m) * a.d, nullptr};
+  if (kind == kRowsE) return RowRef{a.E + size_t(m) * a.d, nullptr};
   if (kind == kRowsPA) {
     const int per = kCand * (a.L - 1) + 1;
     const int b = m / per, q = m % per;
-    tok = q == 0 ? a.verified[b] : a.cand_idx[size_t(b) * a.L * kCand + (q - 1)];
-  } else {
-    const int per = kCand * a.L;
-    const int b = m / per, q = m % per;
-    tok = a.cand_idx[size_t(b) * a.L * kCand + q];
+    return RowRef{nullptr, q == 0 ? a.verified + b : a.cand_idx + size_t(b) * a.L * kCand + (q - 1)};
   }
+  return RowRef{nullptr, a.cand_idx + m};  // PB: row m is candidate m
+}
+// The row of a reference, after the wait; nullptr (a zero row) past M or for a
+// token outside [0, V), which is recorded.
+__device__ __forceinline__ const __nv_bfloat16* a_row_at(const GemmArgs& a, RowRef r) {
+  if (!r.tok) return r.row;
+  const int32_t tok = *r.tok;
   if (tok < 0 || tok >= a.V) {  // never read outside E: record it and use a zero row
     record_error(a.err, kDevErrBadIndex);
     return nullptr;
   }
   return a.E + size_t(tok) * a.d;
 }
+
 
 // WARP = false: tcgen05 MMAs issued by one thread into a TMEM accumulator.
 // WARP = true (CTAs of 128 output columns only): the warp-level engine, each
@@ -150,6 +160,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = WARP ? 0u : *tmem_slot;
+  // the epilogue's index arithmetic (bn / 4 is a power of two; the K split's
+  // row slice of this CTA)
+  const int q4 = bn / 4, q4s = 31 - __clz(q4);
+  const int per = (kBM + a.splits - 1) / a.splits;
+  const int r0 = split * per;
+  const int valid_rows = max(0, min(min(per, kBM - r0), P.M - (m0 + r0)));
+  // the producers' 8 rows, resolved up to the token reads
+  RowRef refs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) refs[i] = a_row_ref(a, P.kind, m0 + ((tid & 127) >> 3) + 16 * i, P.M);
   pdl_wait();  // candidates may come from the previous kernel
 
   if (warp < 4) {
@@ -157,7 +177,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int j = tid & 7;  // 16-byte chunk within the 128-byte row
     const __nv_bfloat16* src[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) src[i] = a_row(a, P.kind, m0 + (tid >> 3) + 16 * i, P.M);
+    for (int i = 0; i < 8; ++i) src[i] = a_row_at(a, refs[i]);
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kGStages;
       if (it >= kGStages && !mbar_wait(&empty_bar[s], ((it / kGStages) - 1) & 1, a.err))
@@ -290,7 +310,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int rows = max(0, min(kBM, P.M - m0));
     const float* stage = reinterpret_cast<const float*>(smem);
     for (int e = tid; e < rows * (bn / 4); e += kGemmThreads) {
-      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      const int lr = e >> q4s, c4 = e & (q4 - 1);
       *reinterpret_cast<float4*>(P.out + size_t(m0 + lr) * kBN + n0 + 4 * c4) =
           *reinterpret_cast<const float4*>(stage + size_t(lr) * (kBN + 4) + 4 * c4);
     }
@@ -335,7 +355,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   {
     const int rows = max(0, min(kBM, P.M - m0));
     for (int e = tid; e < rows * (bn / 4); e += kGemmThreads) {
-      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      const int lr = e >> q4s, c4 = e & (q4 - 1);
       *reinterpret_cast<float4*>(mypart + size_t(m0 + lr) * kBN + n0 + 4 * c4) =
           *reinterpret_cast<const float4*>(stage + size_t(lr) * kStagePitch + 4 * c4);
     }
@@ -348,10 +368,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   // the next launch may start now (it waits for this grid to finish before
   // reading anything, and holds no tensor memory)
   pdl_launch_dependents();
-  const int per = (kBM + S - 1) / S;
-  const int r0 = split * per;
-  const int valid_rows = max(0, min(min(per, kBM - r0), P.M - (m0 + r0)));
-  const int n4 = valid_rows * (bn / 4);
+  const int n4 = valid_rows * q4;
   constexpr int kMaxSplitLoads = kMaxClusterSplits;
   constexpr int kPer = 2;  // elements per thread and pass: 2 x 8 loads in flight
   for (int e0 = tid; e0 < n4; e0 += kGemmThreads * kPer) {
@@ -359,7 +376,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
       const int e = e0 + u * kGemmThreads;
-      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      const int lr = e >> q4s, c4 = e & (q4 - 1);
       const size_t at = size_t(m0 + r0 + lr) * kBN + n0 + 4 * c4;
 #pragma unroll
       for (int k = 0; k < kMaxSplitLoads; ++k)  // every split's value requested first
@@ -371,7 +388,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int u = 0; u < kPer; ++u) {
       const int e = e0 + u * kGemmThreads;
       if (e >= n4) break;
-      const int lr = e / (bn / 4), c4 = e % (bn / 4);
+      const int lr = e >> q4s, c4 = e & (q4 - 1);
       float4 acc = v[u][0];
 #pragma unroll
       for (int k = 1; k < kMaxSplitLoads; ++k) {  // rank order: deterministic
