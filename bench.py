@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4940544,
     ("topk", "serving_b64"): 314891008,
-    ("conv", "drafter4b_l16"): 1761024,
+    ("conv", "drafter4b_l16"): 1766656,
     ("conv", "serving_b64"): 7291136,
     ("lmhead", "drafter4b_l16"): 781673728,
     ("lmhead", "serving_b64"): 786832384,
