@@ -834,8 +834,9 @@ __global__ void __launch_bounds__(kCThreads, 2)
     for (int u = 0; u < kPRun; ++u)
       if (i0 + u < np)
         cur[u] = *reinterpret_cast<const uint4*>(a.x + size_t(pf + u) * a.d + ch0);
+    int tl = pf % a.L, bq = pf / a.L;  // position in its sequence, and the sequence
     uint4 prev = *reinterpret_cast<const uint4*>(
-        (pf % a.L == 0 ? a.x_prev + size_t(pf / a.L) * a.d : a.x + size_t(pf - 1) * a.d) + ch0);
+        (tl == 0 ? a.x_prev + size_t(bq) * a.d : a.x + size_t(pf - 1) * a.d) + ch0);
     float b0[8], b1[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -848,8 +849,11 @@ __global__ void __launch_bounds__(kCThreads, 2)
     for (int u = 0; u < kPRun; ++u) {
       if (i0 + u >= np) break;
       const int pp = pf + u;
-      if (u > 0 && pp % a.L == 0)  // a sequence starts inside the run
-        prev = *reinterpret_cast<const uint4*>(a.x_prev + size_t(pp / a.L) * a.d + ch0);
+      if (u > 0 && ++tl == a.L) {  // a sequence starts inside the run
+        tl = 0;
+        ++bq;
+        prev = *reinterpret_cast<const uint4*>(a.x_prev + size_t(bq) * a.d + ch0);
+      }
       const float c0 = c0p[u], c1 = c1p[u];
       float xt[8], xm[8];
       bf8_unpack(cur[u], xt);
