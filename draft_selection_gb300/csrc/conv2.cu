@@ -670,6 +670,13 @@ __global__ void __launch_bounds__(kCThreads, 2)
   const int nkb = min(a.kblocks, kb0 + a.kps) - kb0;  // >= 1 by construction on the host
   const uint32_t ncols = Np <= 32 ? 32u : (Np <= 64 ? 64u : (Np <= 128 ? 128u : 256u));
   const int gown = g0 + split * og;  // first group this CTA mixes
+  // Index arithmetic of the loops after the mainloop, set up once: og (and so
+  // 2 og) is a power of two (S is), and e / (Np / 4) for e < 2^16 is one
+  // multiply-high by ceil(2^32 / (Np / 4)) (exact while e * (Np / 4) < 2^32).
+  const int ogs = 31 - __clz(og);
+  const uint32_t np4 = uint32_t(Np / 4);
+  const uint64_t np4_inv = ((uint64_t(1) << 32) + np4 - 1) / np4;
+  auto div_np4 = [&](int e) { return int((uint64_t(uint32_t(e)) * np4_inv) >> 32); };
 
   if (tid == 0) {
     for (int st = 0; st < nst; ++st) {
@@ -795,8 +802,8 @@ __global__ void __launch_bounds__(kCThreads, 2)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int e = min(e0 + h * kCThreads, n4 - 1);
-        const int orow = e / (Np / 4), c4 = e % (Np / 4);
-        const int row = (orow / og) * kPGroups + split * og + orow % og;
+        const int orow = div_np4(e), c4 = e - orow * int(np4);
+        const int row = (orow >> ogs) * kPGroups + split * og + (orow & (og - 1));
         const float* src = parts + size_t(row) * Np + 4 * c4;
 #pragma unroll
         for (int k = 0; k < kCMaxSplits; ++k)
@@ -813,7 +820,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
           if (k < S) {
             acc.x += v[h][k].x; acc.y += v[h][k].y; acc.z += v[h][k].z; acc.w += v[h][k].w;
           }
-        const int orow = e / (Np / 4), c4 = e % (Np / 4);
+        const int orow = div_np4(e), c4 = e - orow * int(np4);
         *reinterpret_cast<float4*>(corr + size_t(orow) * pitch + 4 * c4) = acc;
       }
     }
@@ -824,7 +831,7 @@ __global__ void __launch_bounds__(kCThreads, 2)
   const int ncolumn = 2 * og;
   const int items = ncolumn * ((np + kPRun - 1) / kPRun);
   for (int item = tid; item < items; item += kCThreads) {
-    const int col = item % ncolumn, i0 = (item / ncolumn) * kPRun;
+    const int col = item & (ncolumn - 1), i0 = (item >> (ogs + 1)) * kPRun;
     const int gl = col >> 1, h = col & 1, g = gown + gl;
     if (g >= a.G) continue;
     const int ch0 = 16 * g + 8 * h;
