@@ -42,7 +42,7 @@ NCU_TRAFFIC = {
     ("topk", "drafter4b_l16"): 4940544,
     ("topk", "serving_b64"): 314891008,
     ("conv", "drafter4b_l16"): 1766656,
-    ("conv", "serving_b64"): 7291136,
+    ("conv", "serving_b64"): 7283200,
     ("lmhead", "drafter4b_l16"): 781673728,
     ("lmhead", "serving_b64"): 786832384,
 }
